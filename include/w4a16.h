@@ -1,0 +1,127 @@
+/*
+ * w4a16.h - C ABI of the W4A16 group-quantized GEMV/GEMM library (libw4a16.so).
+ *
+ * Weight format (source: "Gemma 4 E2B on a 4 GB GPU with pure PyTorch",
+ * checkpoint paragraph: compressed-tensors W4A16, 4-bit weights in groups of 32
+ * along K, 16-bit activations, each group's step stored in bf16; w4gemv
+ * paragraph: a code c stands for (c - 8) * step, the "subtract 2^23 + 8" unpack):
+ *
+ *   qweight  uint32 [N][K/8]      8 codes per word along K, low nibble first:
+ *                                 code (n,k) = (qweight[n][k/8] >> 4*(k%8)) & 0xF
+ *   scales   bf16   [N][K/group]  raw bf16 bits (uint16_t), row-major
+ *   x        bf16   [M][K]        raw bf16 bits, row-major
+ *   y        fp32   [M][N]        y[m][n] = sum_k x[m][k] * (code(n,k) - 8) * scale(n, k/group)
+ *
+ * Conventions for every call below:
+ *   - Every array pointer is a DEVICE pointer owned by the caller. The library
+ *     never frees, retains or reallocates caller memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Calls only enqueue work on `stream` and return; nothing is
+ *     complete until the caller synchronizes that stream.
+ *   - Arguments are validated on the host before anything is launched. A call
+ *     that returns an error launched nothing.
+ *   - Results are bitwise deterministic run to run (no floating-point atomics).
+ *   - All calls are safe to capture in a CUDA graph once the library has been
+ *     initialised on the device (w4_init, or any earlier call on that device).
+ *   - group must be 32 (the only group size the pages use for this format).
+ *   - K must be a positive multiple of 32; N and M positive; N*K/8 and M*K must
+ *     fit in int32 index space as stated per call.
+ *   - Pointers must be 16-byte aligned (128-bit loads); y must be 4-byte aligned.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4_OK = 0,
+    W4_ERR_INVALID_ARG = 1,  /* NULL pointer, size <= 0, K % group != 0, size overflow */
+    W4_ERR_UNSUPPORTED = 2,  /* group != 32, M beyond what the call serves */
+    W4_ERR_MISALIGNED = 3,   /* a pointer is not aligned as stated above */
+    W4_ERR_CUDA = 4,         /* the CUDA runtime reported an error (launch or allocation) */
+    W4_ERR_NO_DEVICE = 5     /* no usable sm_103 device is current */
+} w4_status;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *w4_status_string(int status);
+
+/* The CUDA error string behind the last W4_ERR_CUDA on this thread ("" if none). */
+const char *w4_last_cuda_error(void);
+
+/*
+ * Set up the library on the current device: checks that it is sm_103 and
+ * allocates the small library-owned scratch the argmax call uses (a few KB,
+ * held until process exit). Idempotent. Call it before capturing any call of
+ * this library in a CUDA graph; otherwise the first call on a device does it.
+ */
+int w4_init(void);
+
+/*
+ * W4A16 matrix-vector product for decode, M in [1, 8].
+ * Source: the w4gemv paragraph (one vector times every weight matrix; packed
+ * words read directly, unpacked in registers, never a 16-bit copy) and the
+ * per-shape tiling paragraph (a fixed tiling per weight shape).
+ *   y [M][N] fp32 out; x [M][K] bf16; qweight [N][K/8]; scales [N][K/32].
+ * The library picks the tiling from (M, N, K). Returns W4_ERR_UNSUPPORTED for
+ * M > 8 (use w4a16_gemm). The kernel honours programmatic dependent launch:
+ * it starts streaming weights before the previous kernel on `stream` has
+ * finished and reads x only after it has.
+ */
+int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+               int M, int N, int K, int group, void *stream);
+
+/*
+ * W4A16 GEMM for any M >= 1. M <= 8 runs the decode kernel of w4a16_gemv; larger
+ * M (prompt reads, the prefill paragraph: a prompt is read in chunks and every
+ * weight multiplies the whole chunk) runs a tensor-core kernel that dequantizes
+ * each weight tile to bf16 (round to nearest even) on its way into shared
+ * memory and accumulates in fp32 in tensor memory. Same layouts as w4a16_gemv.
+ * For M > 8, N must be a multiple of 16 and K a multiple of 64.
+ */
+int w4a16_gemm(float *y, const uint16_t *x, const uint32_t *qweight, const uint16_t *scales,
+               int M, int N, int K, int group, void *stream);
+
+/*
+ * Decode GEMV with a fused greedy pick, M in [1, 8].
+ * Source: Step 2 (the tied 4-bit embedding doubles as the output layer) and the
+ * scope note (greedy decoding): y as w4a16_gemv, and argmax[m] = the lowest n
+ * with y[m][n] equal to the largest y[m][:] (-0 and +0 compare equal; y is the
+ * fp32 value written to y). argmax is a device int32 [M].
+ * Uses the library-owned scratch set up by w4_init; calls that overlap in time on
+ * different streams share it and must not run concurrently.
+ */
+int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32_t *qweight,
+                      const uint16_t *scales, int M, int N, int K, int group, void *stream);
+
+/*
+ * 4-bit row gather (the per-layer embedding lookup on the card, Step 2).
+ *   out    bf16 [M][K] out: out[t][k] = bf16_rne((code(ids[t], k) - 8) * scale)
+ *   ids    int32 [M] device, row indices into the table
+ *   qtable uint32 [N][K/8], scales bf16 [N][K/32]
+ *   status int32 device word or NULL: an id outside [0, N) gives a zero row and,
+ *          if status is not NULL, stores 1 to *status (never cleared by the library).
+ * The product of a 4-bit code and a bf16 step is exact in fp32, so the output is
+ * bit-exact: one rounding, to nearest even.
+ */
+int w4_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qtable,
+                    const uint16_t *scales, int M, int N, int K, int group,
+                    int32_t *status, void *stream);
+
+/*
+ * Memory read probe (the memory-read paragraph: the card's read ceiling measured
+ * by a plain sum over memory). Streams `bytes` of `buf` once and stores the sum of
+ * its uint32 words mod 2^64 to *sum (device uint64). bytes must be a positive
+ * multiple of 16; buf 16-byte aligned. Time it with events on `stream`.
+ */
+int hbm_read_probe(unsigned long long *sum, const void *buf, size_t bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

@@ -1,0 +1,130 @@
+"""ctypes front end of the plain C oracle (test infrastructure only).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg
+import this package. The CUDA library and its Python binding never do.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "w4a16_oracle.c")
+_LIB = os.path.join(_HERE, "libw4a16_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (host-only, portable C, no -march flags)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-Wextra",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        I = ctypes.c_int64
+        lib.w4o_gemm_rows.argtypes = [P, P, P, P, P, I, I, I, I, P, I]
+        lib.w4o_gemm_rows.restype = None
+        lib.w4o_dequant_rows.argtypes = [P, P, P, I, I, I, P, I]
+        lib.w4o_dequant_rows.restype = None
+        lib.w4o_argmax.argtypes = [P, I, P]
+        lib.w4o_argmax.restype = I
+        lib.w4o_embed_gather.argtypes = [P, P, P, P, I, I, I, I, P]
+        lib.w4o_embed_gather.restype = None
+        lib.w4o_sum_words.argtypes = [P, I]
+        lib.w4o_sum_words.restype = ctypes.c_uint64
+        lib.w4o_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.w4o_f32_to_bf16.restype = ctypes.c_uint16
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def gemm(x, qweight, scales, group: int = 32, rows=None):
+    """(y, absy) in fp64. x bf16 bits [M][K]; qweight u32 [N][K/8]; scales bf16 bits [N][K/g].
+
+    rows: optional list of output rows to compute (then y is [M][len(rows)]).
+    """
+    lib = _load()
+    x = _c(np.atleast_2d(x), np.uint16)
+    qweight = _c(qweight, np.uint32)
+    scales = _c(scales, np.uint16)
+    M, K = x.shape
+    N = qweight.shape[0]
+    assert qweight.shape[1] * 8 == K and scales.shape == (N, K // group)
+    if rows is None:
+        r = None
+        nr = N
+    else:
+        r = _c(rows, np.int64)
+        nr = r.shape[0]
+    y = np.empty((M, nr), dtype=np.float64)
+    a = np.empty((M, nr), dtype=np.float64)
+    lib.w4o_gemm_rows(_ptr(y), _ptr(a), _ptr(x), _ptr(qweight), _ptr(scales),
+                      M, N, K, group, None if r is None else _ptr(r), nr)
+    return y, a
+
+
+def dequant(qweight, scales, group: int = 32, rows=None):
+    lib = _load()
+    qweight = _c(qweight, np.uint32)
+    scales = _c(scales, np.uint16)
+    N, K = qweight.shape[0], qweight.shape[1] * 8
+    r = None if rows is None else _c(rows, np.int64)
+    nr = N if r is None else r.shape[0]
+    w = np.empty((nr, K), dtype=np.float64)
+    lib.w4o_dequant_rows(_ptr(w), _ptr(qweight), _ptr(scales), N, K, group,
+                         None if r is None else _ptr(r), nr)
+    return w
+
+
+def argmax(y):
+    """(index, gap) of a 1-D fp64 vector: lowest index of the max, -0 == +0."""
+    lib = _load()
+    y = _c(y, np.float64).ravel()
+    gap = np.zeros(1, dtype=np.float64)
+    idx = lib.w4o_argmax(_ptr(y), y.shape[0], _ptr(gap))
+    return int(idx), float(gap[0])
+
+
+def embed_gather(ids, qtable, scales, group: int = 32):
+    """(out bf16 bits [M][K], flag) for the 4-bit row gather."""
+    lib = _load()
+    ids = _c(ids, np.int32).ravel()
+    qtable = _c(qtable, np.uint32)
+    scales = _c(scales, np.uint16)
+    N, K = qtable.shape[0], qtable.shape[1] * 8
+    out = np.empty((ids.shape[0], K), dtype=np.uint16)
+    flag = np.zeros(1, dtype=np.int32)
+    lib.w4o_embed_gather(_ptr(out), _ptr(ids), _ptr(qtable), _ptr(scales),
+                         ids.shape[0], N, K, group, _ptr(flag))
+    return out, int(flag[0])
+
+
+def sum_words(buf):
+    """Sum of the uint32 words of buf, mod 2^64."""
+    lib = _load()
+    b = _c(buf, np.uint32).ravel()
+    return int(lib.w4o_sum_words(_ptr(b), b.shape[0]))
+
+
+def f32_to_bf16(f: float) -> int:
+    return int(_load().w4o_f32_to_bf16(float(f)))

@@ -1,0 +1,135 @@
+"""Seeded synthetic inputs for the W4A16 path (shared by the oracle tests and the CUDA path).
+
+This module holds no arithmetic of the method itself: it only draws the data that
+both sides consume. Every draw is counter-based, so any slice of a stream can be
+regenerated without the rest.
+
+Generator: SplitMix64 (G. Steele, D. Lea, C. Flood, "Fast splittable pseudorandom
+number generators", OOPSLA 2014). Draw i of the stream with initial state s0 is
+mix(s0 + (i+1) * 0x9E3779B97F4A7C15) with the published 64-bit finaliser.
+Normals: Box-Muller (1958) in fp64 on pairs of 53-bit uniforms.
+
+Distributions (the workload statement of the W4A16 GEMV configs):
+  codes  : the low 32 bits of successive draws are whole uint32 words, so every
+           4-bit code is uniform over 0..15.
+  steps  : bf16(|N(0,1)| * 0.02 + 1e-4), one per group of 32 along K.
+  x      : bf16(N(0,1)).
+  ids    : uniform integers in [0, n_rows).
+Rounding of generated values: fp64 -> fp32 (round to nearest even) -> bf16 (round
+to nearest even). The bf16 bits are the data; both sides consume the same bits.
+
+Stream state: seed * 0x9E3779B97F4A7C15 + tag (mod 2^64), with tag 0 = codes,
+1 = steps, 2 = x (one row), 3 = ids, 4 = x (several rows), 5 = probe buffer.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+GOLDEN_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+TAG_CODES, TAG_STEPS, TAG_X, TAG_IDS, TAG_XROWS, TAG_PROBE = 0, 1, 2, 3, 4, 5
+
+_CHUNK = 1 << 20
+_S27, _S30, _S31 = np.uint64(27), np.uint64(30), np.uint64(31)
+
+
+def stream_state(seed: int, tag: int) -> int:
+    return (seed * 0x9E3779B97F4A7C15 + tag) & 0xFFFFFFFFFFFFFFFF
+
+
+def splitmix64(state0: int, start: int, count: int) -> np.ndarray:
+    """Draws start .. start+count-1 of the SplitMix64 stream with initial state state0."""
+    out = np.empty(count, dtype=np.uint64)
+    s0 = np.uint64(state0)
+    n0 = min(_CHUNK, count)
+    z = np.empty(n0, dtype=np.uint64)
+    t = np.empty(n0, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        for c0 in range(0, count, _CHUNK):
+            n = min(_CHUNK, count - c0)
+            zz, tt = z[:n], t[:n]
+            zz[:] = np.arange(start + c0 + 1, start + c0 + 1 + n, dtype=np.uint64)
+            np.multiply(zz, GOLDEN_GAMMA, out=zz)
+            np.add(zz, s0, out=zz)
+            np.right_shift(zz, _S30, out=tt)
+            np.bitwise_xor(zz, tt, out=zz)
+            np.multiply(zz, _M1, out=zz)
+            np.right_shift(zz, _S27, out=tt)
+            np.bitwise_xor(zz, tt, out=zz)
+            np.multiply(zz, _M2, out=zz)
+            np.right_shift(zz, _S31, out=tt)
+            np.bitwise_xor(zz, tt, out=out[c0:c0 + n])
+    return out
+
+
+def uniform53(state0: int, start: int, count: int) -> np.ndarray:
+    """fp64 uniforms in [0, 1): the top 53 bits of each draw times 2^-53."""
+    return (splitmix64(state0, start, count) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def normals(state0: int, count: int) -> np.ndarray:
+    """count N(0,1) values in fp64 by Box-Muller over consecutive draw pairs."""
+    pairs = (count + 1) // 2
+    out = np.empty(2 * pairs, dtype=np.float64)
+    for p0 in range(0, pairs, _CHUNK):
+        n = min(_CHUNK, pairs - p0)
+        u = uniform53(state0, 2 * p0, 2 * n)
+        u1 = 1.0 - u[0::2]  # (0, 1], keeps log finite
+        u2 = u[1::2]
+        r = np.sqrt(-2.0 * np.log(u1))
+        t = 2.0 * np.pi * u2
+        out[2 * p0:2 * (p0 + n):2] = r * np.cos(t)
+        out[2 * p0 + 1:2 * (p0 + n):2] = r * np.sin(t)
+    return out[:count]
+
+
+def f64_to_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """fp64 -> fp32 (RNE, numpy cast) -> bf16 bits (RNE). Finite inputs only."""
+    u = np.ascontiguousarray(v, dtype=np.float64).astype(np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    with np.errstate(over="ignore"):
+        r = (u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def gen_qweight(seed: int, n: int, k: int) -> np.ndarray:
+    """uint32 [n][k/8]: 8 codes per word, every nibble uniform 0..15."""
+    assert k % 8 == 0
+    w = splitmix64(stream_state(seed, TAG_CODES), 0, n * (k // 8))
+    return (w & np.uint64(0xFFFFFFFF)).astype(np.uint32).reshape(n, k // 8)
+
+
+def gen_scales(seed: int, n: int, k: int, group: int = 32) -> np.ndarray:
+    """bf16 bits [n][k/group]: |N(0,1)| * 0.02 + 1e-4."""
+    assert k % group == 0
+    z = normals(stream_state(seed, TAG_STEPS), n * (k // group))
+    return f64_to_bf16_bits(np.abs(z) * 0.02 + 1e-4).reshape(n, k // group)
+
+
+def gen_x(seed: int, m: int, k: int) -> np.ndarray:
+    """bf16 bits [m][k], N(0,1). One row uses tag 2, several rows tag 4."""
+    tag = TAG_X if m == 1 else TAG_XROWS
+    return f64_to_bf16_bits(normals(stream_state(seed, tag), m * k)).reshape(m, k)
+
+
+def gen_ids(seed: int, count: int, n_rows: int) -> np.ndarray:
+    """int32 [count], uniform in [0, n_rows): (high 32 bits * n_rows) >> 32."""
+    z = splitmix64(stream_state(seed, TAG_IDS), 0, count) >> np.uint64(32)
+    return ((z * np.uint64(n_rows)) >> np.uint64(32)).astype(np.int32)
+
+
+def gen_words(seed: int, nwords: int) -> np.ndarray:
+    """uint32 [nwords] of uniform bits (buffer for the memory read probe)."""
+    w = splitmix64(stream_state(seed, TAG_PROBE), 0, nwords)
+    return (w & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+
+
+def gen_w4_problem(seed: int, m: int, n: int, k: int, group: int = 32):
+    """(x bf16 [m][k], qweight u32 [n][k/8], scales bf16 [n][k/group]) for one projection."""
+    return gen_x(seed, m, k), gen_qweight(seed, n, k), gen_scales(seed, n, k, group)
