@@ -1,0 +1,419 @@
+"""Benchmark: full-model decode weight sweep through the W4A16 GEMV.
+
+Workload (one step): the M=1 decode weight sweep of a 35-layer, hidden-1536
+model: per layer q 2048x1536, k 256x1536, v 256x1536, o 1536x2048, gate and up
+Fx1536, down 1536xF (F = 6144 for layers 0-14, 12288 for 15-34), 4-bit codes in
+groups of 32 with bf16 steps, bf16 activations, fp32 outputs. q|k|v and gate|up
+read the same input and run as one fused call each (140 calls per sweep), in
+per-layer dependency order, replayed as one CUDA graph. Inputs are seeded
+synthetic data (SplitMix64 codes, |N(0,1)|*0.02+1e-4 steps, N(0,1) x).
+
+Metric: GB/s of the sweep (algorithmic bytes: packed codes + steps + x + y,
+divided by the device time of one sweep) and ms per sweep.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the plain CPU oracle (the reference arm of this build)
+on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+HIDDEN = 1536
+LAYERS = 35
+METRIC = "W4A16 GEMV GB/s & % of HBM roofline; ms per full-model decode weight sweep"
+WORKLOAD = ("decode weight sweep, M=1: 35 layers, hidden 1536, q 2048/k 256/v 256/o 1536x2048/"
+            "gate,up Fx1536/down 1536xF, F=6144 (layers 0-14) or 12288 (15-34); W4A16 g32")
+PROJ = ("q", "k", "v", "o", "gate", "up", "down")
+
+
+def ffn(layer: int) -> int:
+    return 6144 if layer < 15 else 12288
+
+
+def layer_shapes(layer: int):
+    """(name, N, K) of the 7 projections of a layer, in decode order."""
+    F = ffn(layer)
+    return [("q", 2048, HIDDEN), ("k", 256, HIDDEN), ("v", 256, HIDDEN), ("o", HIDDEN, 2048),
+            ("gate", F, HIDDEN), ("up", F, HIDDEN), ("down", HIDDEN, F)]
+
+
+def seed_of(layer: int, proj: str) -> int:
+    return 1 + 7 * layer + PROJ.index(proj)
+
+
+def fused_stages(layer: int):
+    """The 4 fused calls of a layer: (name, [member projections], N, K)."""
+    F = ffn(layer)
+    return [("qkv", ["q", "k", "v"], 2560, HIDDEN), ("o", ["o"], HIDDEN, 2048),
+            ("gateup", ["gate", "up"], 2 * F, HIDDEN), ("down", ["down"], HIDDEN, F)]
+
+
+def stage_bytes(N: int, K: int, M: int = 1) -> int:
+    """Algorithmic bytes of one call: codes + steps + x + y."""
+    return N * K // 2 + N * (K // 32) * 2 + M * K * 2 + M * N * 4
+
+
+def sweep_bytes(M: int = 1) -> int:
+    return sum(stage_bytes(N, K, M) for l in range(LAYERS) for _, _, N, K in fused_stages(l))
+
+
+def sweep_weight_bytes() -> int:
+    return sum(N * K // 2 + N * (K // 32) * 2 for l in range(LAYERS) for _, _, N, K in fused_stages(l))
+
+
+# ----------------------------------------------------------------- data ----
+
+class Sweep:
+    """Device-resident sweep: per fused stage one qweight/scales/x/y buffer."""
+
+    def __init__(self, device, keep_host: bool):
+        import torch
+        self.stages = []
+        for l in range(LAYERS):
+            for name, members, N, K in fused_stages(l):
+                qw = torch.empty((N, K // 8), dtype=torch.int32, device=device)
+                sc_host = np.empty((N, K // 32), dtype=np.uint16)
+                r = 0
+                for p in members:
+                    n_p = next(n for nm, n, _ in layer_shapes(l) if nm == p)
+                    synth.gen_qweight_torch(seed_of(l, p), n_p, K, device, out=qw[r:r + n_p])
+                    sc_host[r:r + n_p] = synth.gen_scales(seed_of(l, p), n_p, K)
+                    r += n_p
+                x_host = synth.gen_x(seed_of(l, members[0]), 1, K)
+                st = {"layer": l, "name": name, "N": N, "K": K, "qw": qw,
+                      "sc": torch.from_numpy(sc_host.view(np.int16)).to(device),
+                      "x": torch.from_numpy(x_host.view(np.int16)).to(device),
+                      "y": torch.empty((1, N), dtype=torch.float32, device=device)}
+                if keep_host:
+                    st["qw_h"] = torch.empty(qw.shape, dtype=torch.int32, pin_memory=True)
+                    st["qw_h"].copy_(qw)
+                    st["sc_h"] = torch.from_numpy(sc_host.view(np.int16)).pin_memory()
+                    st["x_h"] = torch.from_numpy(x_host.view(np.int16)).pin_memory()
+                    st["y_h"] = torch.empty((1, N), dtype=torch.float32, pin_memory=True)
+                self.stages.append(st)
+
+    def run(self, w4, stream=None):
+        for st in self.stages:
+            w4.w4a16_gemv(st["x"], st["qw"], st["sc"], out=st["y"], stream=stream)
+
+
+# --------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock and throttle reasons)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------- reference ----
+
+def oracle_sample(budget_s: float = 12.0):
+    """Time the fp64 CPU oracle over whole sweep stages until ~budget_s of work.
+
+    Returns (GB/s of algorithmic sweep bytes, description of the sample, seconds).
+    """
+    import oracle
+    done_bytes, t_total, stages = 0, 0.0, 0
+    order = [(l, s) for l in (0, 15, 1, 16, 2, 17, 3, 18) for s in fused_stages(l)]
+    for l, (name, members, N, K) in order:
+        x = synth.gen_x(seed_of(l, members[0]), 1, K)
+        qws, scs = [], []
+        for p in members:
+            n_p = next(n for nm, n, _ in layer_shapes(l) if nm == p)
+            qws.append(synth.gen_qweight(seed_of(l, p), n_p, K))
+            scs.append(synth.gen_scales(seed_of(l, p), n_p, K))
+        qw, sc = np.concatenate(qws), np.concatenate(scs)
+        t0 = time.perf_counter()
+        oracle.gemm(x, qw, sc)
+        t_total += time.perf_counter() - t0
+        done_bytes += stage_bytes(N, K)
+        stages += 1
+        if t_total >= budget_s:
+            break
+    desc = f"{stages} fused stages of layers 0,15,1,16,... ({done_bytes / 1e6:.1f} MB of the sweep)"
+    return done_bytes / t_total / 1e9, desc, t_total
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    vals = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        gbs, desc, secs = oracle_sample(budget_s=4.0)
+        if i >= args.warmup:
+            vals.append(gbs)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sweep_bytes() / (v * 1e9) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sweep_bytes": sweep_bytes()},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": desc + " per step; ms_per_step extrapolated to the full sweep"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- ours ----
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    from bit_weight_only_w4a16_gb300 import build as _build
+    _build.build()
+    import bit_weight_only_w4a16_gb300 as w4
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w4.init()
+    stream = torch.cuda.Stream(device=dev)
+
+    sweep = Sweep(dev, keep_host=True)
+    nbytes = sweep_bytes()
+    ncalls = len(sweep.stages)
+
+    # Capture the sweep once; every step replays the graph.
+    with torch.cuda.stream(stream):
+        sweep.run(w4, stream)  # warm the library (and any lazy set-up) outside capture
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        sweep.run(w4, stream)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        with torch.cuda.stream(stream):
+            g.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    t_ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([t_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_ms = float(t.item())
+    value = world * nbytes / (t_ms * 1e-3) / 1e9
+
+    # In-run read ceiling: the plain-sum probe over a 4 GiB buffer.
+    probe_buf = torch.empty(1 << 30, dtype=torch.int32, device=dev)
+    probe_buf.fill_(1)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            w4.hbm_read_probe(probe_buf, stream=stream)
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for _ in range(10):
+            w4.hbm_read_probe(probe_buf, stream=stream)
+        p1.record(stream)
+    torch.cuda.synchronize()
+    probe_gbs = probe_buf.numel() * 4 / (p0.elapsed_time(p1) / 10 * 1e-3) / 1e9
+    del probe_buf
+    torch.cuda.empty_cache()
+
+    # End to end through the public call with host buffers: every step copies
+    # the sweep's packed weights, steps and x from pinned host memory and reads
+    # every y back. Copies of stage s+1 overlap the GEMV of stage s.
+    e2e = None
+    if args.e2e:
+        cstream = torch.cuda.Stream(device=dev)
+        h2d = sum(st["qw_h"].numel() * 4 + st["sc_h"].numel() * 2 + st["x_h"].numel() * 2
+                  for st in sweep.stages)
+        d2h = sum(st["y_h"].numel() * 4 for st in sweep.stages)
+
+        def e2e_step():
+            ready = []
+            for st in sweep.stages:
+                with torch.cuda.stream(cstream):
+                    st["qw"].copy_(st["qw_h"], non_blocking=True)
+                    st["sc"].copy_(st["sc_h"], non_blocking=True)
+                    st["x"].copy_(st["x_h"], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(cstream)
+                    ready.append(e)
+            for st, e in zip(sweep.stages, ready):
+                stream.wait_event(e)
+                with torch.cuda.stream(stream):
+                    w4.w4a16_gemv(st["x"], st["qw"], st["sc"], out=st["y"], stream=stream)
+                    st["y_h"].copy_(st["y"], non_blocking=True)
+            cstream.wait_stream(stream)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(2, min(args.steps, 10))
+        cstream.wait_stream(stream)
+        q0.record(cstream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        stream.wait_stream(cstream)
+        q1.record(stream)
+        torch.cuda.synchronize()
+        te = q0.elapsed_time(q1) / e2e_steps
+        if world > 1:
+            t = torch.tensor([te], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            te = float(t.item())
+        e2e = {"value": world * nbytes / (te * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": te,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, desc, secs = oracle_sample()
+        cpu = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": desc + f", {secs:.1f} s single-threaded fp64"}
+
+    peak, peak_src = measured_peaks()
+    achieved = nbytes / (t_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": t_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x int4 -> f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "calls_per_sweep": ncalls, "fused": "q|k|v and gate|up",
+                   "launch": "one CUDA graph per sweep, programmatic dependent launch",
+                   "sweep_bytes": nbytes, "weight_bytes": sweep_weight_bytes(),
+                   "l2": "inputs larger than L2 (1.02 GB per sweep vs 129 MB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "kernel": "gemv_m2_kernel (all 140 launches of the sweep)"},
+        "probe": {"hbm_read_probe_gbs": probe_gbs, "sweep_frac_of_probe": achieved / probe_gbs},
+        "gpu_launches": ncalls * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

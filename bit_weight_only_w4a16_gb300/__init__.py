@@ -1,0 +1,168 @@
+"""Python binding of libw4a16.so, the W4A16 GEMV/GEMM library for GB300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/w4a16.h. Tensors must be CUDA
+tensors on the current device; bf16 data may be passed either as torch.bfloat16
+or as raw int16/uint16 bits. There is no CPU path: if the compiled library is
+missing, importing the binding raises.
+
+Weight format: qweight uint32 [N][K/8] (8 codes per word along K, low nibble
+first, zero point 8), scales bf16 [N][K/32], x bf16 [M][K], y fp32 [M][N].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw4a16.so")
+
+W4_OK = 0
+STATUS_NAMES = {0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED",
+                3: "W4_ERR_MISALIGNED", 4: "W4_ERR_CUDA", 5: "W4_ERR_NO_DEVICE"}
+
+# Symbols declared in include/w4a16.h.
+EXPORTS = ("w4_status_string", "w4_last_cuda_error", "w4_init", "w4a16_gemv", "w4a16_gemm",
+           "w4a16_gemv_argmax", "w4_embed_gather", "hbm_read_probe")
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status: int, call: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{call} -> {STATUS_NAMES.get(status, status)}" + (f" ({detail})" if detail else ""))
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with bit_weight_only_w4a16_gb300.build.build() "
+                          "(nvcc, sm_103a). There is no CPU fallback.")
+    lib = ctypes.CDLL(path)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.w4_status_string.argtypes = [I]
+    lib.w4_status_string.restype = ctypes.c_char_p
+    lib.w4_last_cuda_error.argtypes = []
+    lib.w4_last_cuda_error.restype = ctypes.c_char_p
+    lib.w4_init.argtypes = []
+    lib.w4_init.restype = I
+    for name in ("w4a16_gemv", "w4a16_gemm"):
+        f = getattr(lib, name)
+        f.argtypes = [P, P, P, P, I, I, I, I, P]
+        f.restype = I
+    lib.w4a16_gemv_argmax.argtypes = [P, P, P, P, P, I, I, I, I, P]
+    lib.w4a16_gemv_argmax.restype = I
+    lib.w4_embed_gather.argtypes = [P, P, P, P, I, I, I, I, P, P]
+    lib.w4_embed_gather.restype = I
+    lib.hbm_read_probe.argtypes = [P, P, S, P]
+    lib.hbm_read_probe.restype = I
+    return lib
+
+
+_lib = load_library()
+
+
+def _check(rc: int, call: str):
+    if rc != W4_OK:
+        detail = _lib.w4_last_cuda_error().decode() if rc == 4 else ""
+        raise W4Error(rc, call, detail)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _bits16(t, name):
+    _cuda(t, name)
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"{name} must be bf16 (or its raw 16-bit bits)")
+    return t
+
+
+def _u32(t, name):
+    _cuda(t, name)
+    if t.dtype not in (torch.int32, torch.uint32):
+        raise TypeError(f"{name} must be a 32-bit integer tensor of packed words")
+    return t
+
+
+def init():
+    """Set up the library on the current device (call before CUDA graph capture)."""
+    _check(_lib.w4_init(), "w4_init")
+
+
+def _shape(x, qweight, scales, group):
+    M, K = x.shape
+    N = qweight.shape[0]
+    if qweight.shape[1] * 8 != K or tuple(scales.shape) != (N, K // group):
+        raise ValueError(f"shape mismatch: x {tuple(x.shape)}, qweight {tuple(qweight.shape)}, "
+                         f"scales {tuple(scales.shape)}")
+    return M, N, K
+
+
+def w4a16_gemv(x, qweight, scales, group: int = 32, out=None, stream=None):
+    """y[M][N] fp32 = x[M][K] @ dequant(qweight, scales)^T for M <= 8 (decode)."""
+    _bits16(x, "x"); _u32(qweight, "qweight"); _bits16(scales, "scales")
+    M, N, K = _shape(x, qweight, scales, group)
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if out is None else _cuda(out, "out")
+    _check(_lib.w4a16_gemv(_ptr(y), _ptr(x), _ptr(qweight), _ptr(scales), M, N, K, group,
+                           _stream(stream)), "w4a16_gemv")
+    return y
+
+
+def w4a16_gemm(x, qweight, scales, group: int = 32, out=None, stream=None):
+    """y[M][N] fp32 for any M (M > 8 runs the tensor-core prefill kernel)."""
+    _bits16(x, "x"); _u32(qweight, "qweight"); _bits16(scales, "scales")
+    M, N, K = _shape(x, qweight, scales, group)
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if out is None else _cuda(out, "out")
+    _check(_lib.w4a16_gemm(_ptr(y), _ptr(x), _ptr(qweight), _ptr(scales), M, N, K, group,
+                           _stream(stream)), "w4a16_gemm")
+    return y
+
+
+def w4a16_gemv_argmax(x, qweight, scales, group: int = 32, out=None, argmax=None, stream=None):
+    """(y fp32 [M][N], argmax int32 [M]): decode GEMV with the greedy pick fused."""
+    _bits16(x, "x"); _u32(qweight, "qweight"); _bits16(scales, "scales")
+    M, N, K = _shape(x, qweight, scales, group)
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if out is None else _cuda(out, "out")
+    a = torch.empty((M,), dtype=torch.int32, device=x.device) if argmax is None else _cuda(argmax, "argmax")
+    _check(_lib.w4a16_gemv_argmax(_ptr(y), _ptr(a), _ptr(x), _ptr(qweight), _ptr(scales), M, N, K,
+                                  group, _stream(stream)), "w4a16_gemv_argmax")
+    return y, a
+
+
+def w4_embed_gather(ids, qtable, scales, group: int = 32, out=None, status=None, stream=None):
+    """bf16 [M][K] rows of the 4-bit table for int32 ids [M] (raw bits as int16)."""
+    _cuda(ids, "ids"); _u32(qtable, "qtable"); _bits16(scales, "scales")
+    if ids.dtype != torch.int32:
+        raise TypeError("ids must be int32")
+    M = ids.numel()
+    N, K = qtable.shape[0], qtable.shape[1] * 8
+    if tuple(scales.shape) != (N, K // group):
+        raise ValueError("scales shape mismatch")
+    o = torch.empty((M, K), dtype=torch.bfloat16, device=ids.device) if out is None else _cuda(out, "out")
+    _check(_lib.w4_embed_gather(_ptr(o), _ptr(ids), _ptr(qtable), _ptr(scales), M, N, K, group,
+                                _ptr(status), _stream(stream)), "w4_embed_gather")
+    return o
+
+
+def hbm_read_probe(buf, out=None, stream=None):
+    """Device uint64 (as int64) sum of buf's uint32 words mod 2^64 (one streaming read)."""
+    _cuda(buf, "buf")
+    nbytes = buf.numel() * buf.element_size()
+    s = torch.empty((1,), dtype=torch.int64, device=buf.device) if out is None else _cuda(out, "out")
+    _check(_lib.hbm_read_probe(_ptr(s), _ptr(buf), nbytes, _stream(stream)), "hbm_read_probe")
+    return s

@@ -1,0 +1,236 @@
+// C ABI of libw4a16.so: argument validation, per-device set-up and dispatch.
+// The declarations, with the meaning, layout, ownership and error behaviour of
+// every argument, are in include/w4a16.h.
+#include "../../include/w4a16.h"
+#include "internal.h"
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// Argmax scratch: one 64-bit key per (x-row, CTA); 8 rows x 65536 CTAs.
+constexpr size_t kKeyCapacity = 8u * 65536u;
+
+struct DeviceState {
+    bool ready = false;
+    int num_sms = 0;
+    unsigned long long *keys = nullptr;
+};
+
+DeviceState g_dev[kMaxDevices];
+std::mutex g_mu;
+thread_local char g_cuda_err[256] = "";
+
+int cuda_fail(cudaError_t e)
+{
+    std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s", cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+    return W4_ERR_CUDA;
+}
+
+// Set up (once) and return the state of the current device.
+int device_state(DeviceState **out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return W4_ERR_NO_DEVICE;
+    }
+    if (dev < 0 || dev >= kMaxDevices)
+        return W4_ERR_NO_DEVICE;
+    DeviceState &st = g_dev[dev];
+    if (st.ready) {
+        *out = &st;
+        return W4_OK;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!st.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return W4_ERR_NO_DEVICE;
+        }
+        if (major != 10 || minor != 3)
+            return W4_ERR_NO_DEVICE; // kernels are built for sm_103a only
+        void *p = nullptr;
+        e = cudaMalloc(&p, kKeyCapacity * sizeof(unsigned long long));
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+        st.keys = static_cast<unsigned long long *>(p);
+        st.num_sms = sms;
+        st.ready = true;
+    }
+    *out = &st;
+    return W4_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_w4_args(const void *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int M,
+                  int N, int K, int group)
+{
+    if (!y || !x || !qw || !sc)
+        return W4_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0)
+        return W4_ERR_INVALID_ARG;
+    if (group != 32)
+        return W4_ERR_UNSUPPORTED;
+    if (K % group != 0)
+        return W4_ERR_INVALID_ARG;
+    // Every flat index the kernels form stays below 2^31 words or elements.
+    if ((long long)N * (K / 8) >= (1ll << 31) || (long long)M * K >= (1ll << 31) ||
+        (long long)M * N >= (1ll << 31))
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(qw, 16) || !aligned(sc, 4) || !aligned(y, 4))
+        return W4_ERR_MISALIGNED;
+    return W4_OK;
+}
+
+// Shared memory the decode kernels need for x staging; bounded by the SM's 227 KB.
+bool decode_fits(const w4::DecodePlan &p, int M, int K)
+{
+    const int rbc = p.warps / p.ksplit;
+    size_t smem;
+    if (p.kernel == 2)
+        smem = (size_t)M * ((K + 127) / 128 * 128) * 2 + 16 + (size_t)rbc * p.ksplit * M * 64;
+    else
+        smem = (size_t)8 * K * 2 + (size_t)rbc * p.ksplit * 8 * 64;
+    return smem <= 220 * 1024;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *w4_status_string(int status)
+{
+    switch (status) {
+    case W4_OK: return "W4_OK";
+    case W4_ERR_INVALID_ARG: return "W4_ERR_INVALID_ARG";
+    case W4_ERR_UNSUPPORTED: return "W4_ERR_UNSUPPORTED";
+    case W4_ERR_MISALIGNED: return "W4_ERR_MISALIGNED";
+    case W4_ERR_CUDA: return "W4_ERR_CUDA";
+    case W4_ERR_NO_DEVICE: return "W4_ERR_NO_DEVICE";
+    default: return "W4_ERR_UNKNOWN";
+    }
+}
+
+const char *w4_last_cuda_error(void) { return g_cuda_err; }
+
+int w4_init(void)
+{
+    DeviceState *st = nullptr;
+    return device_state(&st);
+}
+
+int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint16_t *scales, int M,
+               int N, int K, int group, void *stream)
+{
+    int rc = check_w4_args(y, x, qweight, scales, M, N, K, group);
+    if (rc != W4_OK)
+        return rc;
+    if (M > 8)
+        return W4_ERR_UNSUPPORTED;
+    DeviceState *st = nullptr;
+    if ((rc = device_state(&st)) != W4_OK)
+        return rc;
+    const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
+    if (!decode_fits(p, M, K))
+        return W4_ERR_UNSUPPORTED;
+    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, nullptr, nullptr,
+                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int w4a16_gemm(float *y, const uint16_t *x, const uint32_t *qweight, const uint16_t *scales, int M,
+               int N, int K, int group, void *stream)
+{
+    if (M >= 1 && M <= 8)
+        return w4a16_gemv(y, x, qweight, scales, M, N, K, group, stream);
+    int rc = check_w4_args(y, x, qweight, scales, M, N, K, group);
+    if (rc != W4_OK)
+        return rc;
+    if (N % 16 != 0 || K % 64 != 0)
+        return W4_ERR_UNSUPPORTED;
+    DeviceState *st = nullptr;
+    if ((rc = device_state(&st)) != W4_OK)
+        return rc;
+    cudaError_t e = w4::run_prefill(y, x, qweight, scales, M, N, K, st->num_sms,
+                                    static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported)
+        return W4_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32_t *qweight,
+                      const uint16_t *scales, int M, int N, int K, int group, void *stream)
+{
+    int rc = check_w4_args(y, x, qweight, scales, M, N, K, group);
+    if (rc != W4_OK)
+        return rc;
+    if (!argmax)
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(argmax, 4))
+        return W4_ERR_MISALIGNED;
+    if (M > 8)
+        return W4_ERR_UNSUPPORTED;
+    DeviceState *st = nullptr;
+    if ((rc = device_state(&st)) != W4_OK)
+        return rc;
+    const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
+    if (!decode_fits(p, M, K) || (size_t)M * p.grid > kKeyCapacity)
+        return W4_ERR_UNSUPPORTED;
+    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, st->keys, argmax,
+                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int w4_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qtable,
+                    const uint16_t *scales, int M, int N, int K, int group, int32_t *status,
+                    void *stream)
+{
+    if (!out || !ids || !qtable || !scales)
+        return W4_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0)
+        return W4_ERR_INVALID_ARG;
+    if (group != 32)
+        return W4_ERR_UNSUPPORTED;
+    if (K % group != 0)
+        return W4_ERR_INVALID_ARG;
+    if ((long long)N * (K / 8) >= (1ll << 31) || (long long)M * K >= (1ll << 31))
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(qtable, 4) || !aligned(scales, 2) || !aligned(ids, 4) ||
+        (status && !aligned(status, 4)))
+        return W4_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != W4_OK)
+        return rc;
+    cudaError_t e = w4::run_embed_gather(out, ids, qtable, scales, M, N, K, status,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int hbm_read_probe(unsigned long long *sum, const void *buf, size_t bytes, void *stream)
+{
+    if (!sum || !buf || bytes == 0)
+        return W4_ERR_INVALID_ARG;
+    if (bytes % 16 != 0)
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(buf, 16) || !aligned(sum, 8))
+        return W4_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != W4_OK)
+        return rc;
+    cudaError_t e = w4::run_read_probe(sum, buf, bytes, st->num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+} // extern "C"

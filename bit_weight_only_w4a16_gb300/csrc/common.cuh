@@ -1,0 +1,133 @@
+// Shared device helpers of the W4A16 CUDA library (sm_103a only).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+// ---------------------------------------------------------------- loads ----
+
+// Streaming 128-bit load of weights: read-only path, not kept in L1, and L2
+// asked to fetch the surrounding 256 B so the next k-tiles of the row hit L2.
+__device__ __forceinline__ uint4 ldg_stream_v4(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Read-only load that may stay in L1 (scales: neighbouring lanes share sectors).
+__device__ __forceinline__ uint32_t ldg_nc_u32(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_nc_u16(const void *p)
+{
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return (uint32_t)v;
+}
+
+// ------------------------------------------------- programmatic launch ----
+
+// Let the next kernel on the stream start launching (its own wait still
+// blocks until this grid has completed and its writes are visible).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Block until every prerequisite grid has completed and its memory is visible.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ------------------------------------------------------------- unpack ----
+
+// Two 4-bit codes, at bits 0..3 and 16..19 of w, as an exact bf16x2 of (code - 8).
+// 0x4300 | c is the bf16 of 128 + c (c fits the 7-bit mantissa); subtracting
+// 136 leaves c - 8 in [-8, 7], which bf16 holds exactly. This is the bf16 form
+// of the "OR into the bits of 2^23 and subtract 2^23 + 8" unpack.
+__device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w)
+{
+    uint32_t t = (w & 0x000F000Fu) | 0x43004300u;
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x43084308u));
+    return r;
+}
+
+// The four bf16x2 pairs of one packed word: nibbles (0,4), (1,5), (2,6), (3,7).
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t &p04, uint32_t &p15,
+                                            uint32_t &p26, uint32_t &p37)
+{
+    p04 = nib_pair_bf16(w);
+    p15 = nib_pair_bf16(w >> 4);
+    p26 = nib_pair_bf16(w >> 8);
+    p37 = nib_pair_bf16(w >> 12);
+}
+
+// x permuted for the B operand: one 8-code word k0..k7 pairs as
+// (x0,x4) (x1,x5) (x2,x6) (x3,x7), matching unpack_word's pairs.
+__device__ __forceinline__ uint4 permute_x8(uint4 in)
+{
+    uint4 o;
+    o.x = __byte_perm(in.x, in.z, 0x5410);
+    o.y = __byte_perm(in.x, in.z, 0x7632);
+    o.z = __byte_perm(in.y, in.w, 0x5410);
+    o.w = __byte_perm(in.y, in.w, 0x7632);
+    return o;
+}
+
+// ---------------------------------------------------------- tensor core ----
+
+// D = A(16x16 bf16) * B(16x8 bf16) + C, fp32 accumulate (warp-level mma).
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// ------------------------------------------------------------- argmax ----
+
+// Order-preserving 64-bit key of (value, index): a larger value wins, and for
+// equal values the lower index wins. -0 is folded into +0 first.
+__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx)
+{
+    uint32_t u = __float_as_uint(v);
+    if (u == 0x80000000u)
+        u = 0u;
+    uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+
+__device__ __forceinline__ uint32_t argmax_key_index(unsigned long long key)
+{
+    return 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b)
+{
+    return a > b ? a : b;
+}
+
+} // namespace w4

@@ -1,0 +1,497 @@
+// Decode-form W4A16 GEMV/GEMM (M = 1..8) on the warp-level tensor core.
+//
+// Source: "Gemma 4 E2B on a 4 GB GPU with pure PyTorch" - the w4gemv paragraph
+// (decode multiplies one vector by every weight matrix, so the speed limit is
+// reading the weights; the kernel reads the packed 4-bit words, unpacks them in
+// registers and multiplies, never writing a 16-bit copy) and the tiling
+// paragraph (each weight shape gets its own fixed tiling).
+//
+// GB300 design. At ~6.8 TB/s and 0.5625 B per weight the kernel must consume
+// ~12e12 weights/s, i.e. ~3 lane-instructions per weight at 2 GHz over 152 SMs.
+// A CUDA-core dot product (unpack + convert + FMA per weight) does not fit, so
+// every 16x16 block of exact (code - 8) values goes to one m16n8k16 bf16 mma
+// with fp32 accumulation; the unpack is ~1.4 instructions per weight.
+// The group step is applied in fp32 after the mma, per group, which keeps the
+// result within 1e-4 of the exact sum (no bf16 rounding of weights).
+//
+// Kernel "m2" (M = 1 or 2): lane (g, t) of a warp loads one full group (32
+// codes, 16 B) of rows g and g+8, group 4*kt + t of k-tile kt, with one 128-bit
+// load each. The four lanes of a quad therefore hold four different groups, and
+// the mma's eight B columns separate them: column 4*m + s carries x-row m
+// restricted to group-slot s (zero elsewhere). After the 8 mmas of a k-tile,
+// C[row][4m+s] is the unscaled partial of (row, group 4kt+s, x-row m), which is
+// scaled in fp32 and accumulated.
+//
+// Kernel "m8" (M = 3..8): lane (g, t) loads word t of one group for rows g and
+// g+8 (32-bit loads); B columns are the x rows; one group per two mmas.
+//
+// Both kernels issue their first weight loads before griddepcontrol.wait, so
+// under programmatic dependent launch the weight stream of this call overlaps
+// the tail of the previous kernel; x is read only after the wait.
+#include "common.cuh"
+#include "internal.h"
+
+namespace w4 {
+
+static constexpr int kTileK = 128; // k per tile of the m2 kernel: 4 groups
+
+// ---------------------------------------------------------------- m2 ----
+
+template <int MX, int U, bool SC32, bool ARGMAX>
+__global__ void __launch_bounds__(512)
+gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+               const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
+               int N, int K, int ksplit, unsigned long long *__restrict__ keys)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int nwarps = blockDim.x >> 5;
+    const int rbc = nwarps / ksplit;
+    const int ks = warp % ksplit, rbl = warp / ksplit;
+    const int nrb = (N + 15) >> 4;
+    const int rb = blockIdx.x * rbc + rbl;
+    const bool active = rb < nrb;
+    const int T = (K + kTileK - 1) / kTileK;
+    const int ngroups = K >> 5;
+    const int Kpad = T * kTileK;
+    const int kt0 = (int)((long long)T * ks / ksplit);
+    const int nkt = (int)((long long)T * (ks + 1) / ksplit) - kt0;
+
+    const int rowA = rb * 16 + g, rowB = rowA + 8;
+    const int rA = min(rowA, N - 1), rB = min(rowB, N - 1);
+    const uint32_t *qA = qw + (size_t)rA * (K >> 3) + 4 * t;
+    const uint32_t *qB = qw + (size_t)rB * (K >> 3) + 4 * t;
+    const uint16_t *sA = sc + (size_t)rA * ngroups + 2 * (t & 1);
+    const uint16_t *sB = sc + (size_t)rB * ngroups + 2 * (t & 1);
+
+    uint4 wa[U], wb[U];
+    uint32_t sa[U], sb[U];
+
+    auto load = [&](int u, int kt) {
+        const int G = 4 * kt + t;
+        if (active && G < ngroups) {
+            wa[u] = ldg_stream_v4(qA + 16 * kt);
+            wb[u] = ldg_stream_v4(qB + 16 * kt);
+        } else {
+            wa[u] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+            wb[u] = wa[u];
+        }
+        const int Gs = 4 * kt + 2 * (t & 1);
+        if (SC32) {
+            const bool ok = active && Gs < ngroups;
+            sa[u] = ok ? ldg_nc_u32(sA + 4 * kt) : 0u;
+            sb[u] = ok ? ldg_nc_u32(sB + 4 * kt) : 0u;
+        } else {
+            const bool ok0 = active && Gs < ngroups, ok1 = active && Gs + 1 < ngroups;
+            sa[u] = (ok0 ? ldg_nc_u16(sA + 4 * kt) : 0u) | ((ok1 ? ldg_nc_u16(sA + 4 * kt + 1) : 0u) << 16);
+            sb[u] = (ok0 ? ldg_nc_u16(sB + 4 * kt) : 0u) | ((ok1 ? ldg_nc_u16(sB + 4 * kt + 1) : 0u) << 16);
+        }
+    };
+
+    // Stream the first weight tiles before waiting on the previous kernel.
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (u < nkt)
+            load(u, kt0 + u);
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // Stage x, permuted into the B-operand pair order, and a zero chunk.
+    uint4 *xs = reinterpret_cast<uint4 *>(smem);
+    const int chunks_per_row = Kpad >> 3;
+    for (int i = threadIdx.x; i < MX * chunks_per_row; i += blockDim.x) {
+        const int m = i / chunks_per_row, c = i - m * chunks_per_row;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (c * 8 < K)
+            v = permute_x8(*reinterpret_cast<const uint4 *>(x + (size_t)m * K + c * 8));
+        xs[i] = v;
+    }
+    uint4 *zero_chunk = xs + MX * chunks_per_row;
+    if (threadIdx.x == 0)
+        *zero_chunk = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+
+    // This lane feeds B column g: x-row g>>2 restricted to group-slot g&3,
+    // which lives on lanes with t == g&3.
+    const int bm = g >> 2;
+    const bool bsel = ((g & 3) == t) && (bm < MX);
+    const uint4 *xrow = bsel ? xs + bm * chunks_per_row + 4 * t : zero_chunk;
+    const int xstep = bsel ? 16 : 0; // chunks per k-tile
+    const int xi = bsel ? 1 : 0;     // chunk stride between words
+
+    float accA = 0.f, accB = 0.f;
+
+    auto compute = [&](int u, int kt) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4 *xb = xrow + xstep * kt;
+        const uint32_t a_w[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+        const uint32_t b_w[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 b = xb[xi * i];
+            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+            unpack_word(a_w[i], a04, a15, a26, a37);
+            unpack_word(b_w[i], b04, b15, b26, b37);
+            mma_16816(c, a04, b04, a15, b15, b.x, b.y);
+            mma_16816(c, a26, b26, a37, b37, b.z, b.w);
+        }
+        accA = fmaf(bf16lo_to_f32(sa[u]), c[0], accA);
+        accA = fmaf(bf16hi_to_f32(sa[u]), c[1], accA);
+        accB = fmaf(bf16lo_to_f32(sb[u]), c[2], accB);
+        accB = fmaf(bf16hi_to_f32(sb[u]), c[3], accB);
+    };
+
+    for (int base = 0; base < nkt; base += U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (base + u < nkt) {
+                compute(u, kt0 + base + u);
+                if (base + u + U < nkt)
+                    load(u, kt0 + base + u + U);
+            }
+        }
+    }
+
+    // Lanes t and t^1 hold the two group-slot pairs of the same (row, x-row).
+    accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
+    accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+    const int m = t >> 1;
+    const bool writer = ((t & 1) == 0) && (m < MX);
+
+    __shared__ unsigned long long ck[MX];
+    if (ARGMAX) {
+        if (threadIdx.x < MX)
+            ck[threadIdx.x] = 0ull;
+        __syncthreads();
+    }
+
+    if (ksplit == 1) {
+        if (writer && active) {
+            if (rowA < N) {
+                y[(size_t)m * N + rowA] = accA;
+                if (ARGMAX)
+                    atomicMax(&ck[m], argmax_key(accA, rowA));
+            }
+            if (rowB < N) {
+                y[(size_t)m * N + rowB] = accB;
+                if (ARGMAX)
+                    atomicMax(&ck[m], argmax_key(accB, rowB));
+            }
+        }
+    } else {
+        // Fixed-order reduction of the k-slices through shared memory.
+        float *red = reinterpret_cast<float *>(zero_chunk + 1); // [rbc][ksplit][MX][16]
+        if (writer) {
+            float *r = red + ((rbl * ksplit + ks) * MX + m) * 16;
+            r[g] = accA;
+            r[g + 8] = accB;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < rbc * MX * 16; i += blockDim.x) {
+            const int rr = i & 15, mm = (i >> 4) % MX, rl = i / (16 * MX);
+            const int row = (blockIdx.x * rbc + rl) * 16 + rr;
+            float s = 0.f;
+            for (int k2 = 0; k2 < ksplit; ++k2)
+                s += red[((rl * ksplit + k2) * MX + mm) * 16 + rr];
+            if (row < N) {
+                y[(size_t)mm * N + row] = s;
+                if (ARGMAX)
+                    atomicMax(&ck[mm], argmax_key(s, row));
+            }
+        }
+    }
+
+    if (ARGMAX) {
+        __syncthreads();
+        if (threadIdx.x < MX)
+            keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
+    }
+}
+
+// ---------------------------------------------------------------- m8 ----
+
+template <int U, bool ARGMAX>
+__global__ void __launch_bounds__(512)
+gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+               const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
+               int M, int N, int K, int ksplit, unsigned long long *__restrict__ keys)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int nwarps = blockDim.x >> 5;
+    const int rbc = nwarps / ksplit;
+    const int ks = warp % ksplit, rbl = warp / ksplit;
+    const int nrb = (N + 15) >> 4;
+    const int rb = blockIdx.x * rbc + rbl;
+    const bool active = rb < nrb;
+    const int ngroups = K >> 5;
+    const int G0 = (int)((long long)ngroups * ks / ksplit);
+    const int nG = (int)((long long)ngroups * (ks + 1) / ksplit) - G0;
+
+    const int rowA = rb * 16 + g, rowB = rowA + 8;
+    const int rA = min(rowA, N - 1), rB = min(rowB, N - 1);
+    const uint32_t *qA = qw + (size_t)rA * (K >> 3) + t;
+    const uint32_t *qB = qw + (size_t)rB * (K >> 3) + t;
+    const uint16_t *sA = sc + (size_t)rA * ngroups;
+    const uint16_t *sB = sc + (size_t)rB * ngroups;
+
+    uint32_t wa[U], wb[U], sa[U], sb[U];
+    auto load = [&](int u, int G) {
+        if (active) {
+            wa[u] = ldg_stream_u32(qA + 4 * G);
+            wb[u] = ldg_stream_u32(qB + 4 * G);
+            sa[u] = ldg_nc_u16(sA + G);
+            sb[u] = ldg_nc_u16(sB + G);
+        } else {
+            wa[u] = wb[u] = 0x88888888u;
+            sa[u] = sb[u] = 0u;
+        }
+    };
+
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (u < nG)
+            load(u, G0 + u);
+    pdl_launch_dependents();
+    pdl_wait();
+
+    uint4 *xs = reinterpret_cast<uint4 *>(smem); // [8][K/8] permuted chunks
+    const int cpr = K >> 3;
+    for (int i = threadIdx.x; i < 8 * cpr; i += blockDim.x) {
+        const int m = i / cpr, c = i - m * cpr;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (m < M)
+            v = permute_x8(*reinterpret_cast<const uint4 *>(x + (size_t)m * K + c * 8));
+        xs[i] = v;
+    }
+    __syncthreads();
+
+    // B column g is x-row g; this lane supplies word t of each group.
+    const uint4 *xrow = xs + g * cpr + t;
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+
+    auto compute = [&](int u, int G) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4 bx = xrow[4 * G];
+        uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+        unpack_word(wa[u], a04, a15, a26, a37);
+        unpack_word(wb[u], b04, b15, b26, b37);
+        mma_16816(c, a04, b04, a15, b15, bx.x, bx.y);
+        mma_16816(c, a26, b26, a37, b37, bx.z, bx.w);
+        const float s_a = bf16lo_to_f32(sa[u]), s_b = bf16lo_to_f32(sb[u]);
+        a0 = fmaf(s_a, c[0], a0);
+        a1 = fmaf(s_a, c[1], a1);
+        b0 = fmaf(s_b, c[2], b0);
+        b1 = fmaf(s_b, c[3], b1);
+    };
+
+    for (int base = 0; base < nG; base += U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (base + u < nG) {
+                compute(u, G0 + base + u);
+                if (base + u + U < nG)
+                    load(u, G0 + base + u + U);
+            }
+        }
+    }
+
+    // Lane (g, t) holds y[2t][rowA], y[2t+1][rowA], y[2t][rowB], y[2t+1][rowB].
+    // CTA-best argmax key per x-row; max is order-independent, so deterministic.
+    __shared__ unsigned long long ck[8];
+    if (ARGMAX) {
+        if (threadIdx.x < 8)
+            ck[threadIdx.x] = 0ull;
+        __syncthreads();
+    }
+    const int m0 = 2 * t, m1 = 2 * t + 1;
+    if (ksplit == 1) {
+        if (active) {
+            const float v[2][2] = {{a0, a1}, {b0, b1}};
+            const int rows[2] = {rowA, rowB};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int mm = j ? m1 : m0;
+                    if (rows[h] < N && mm < M) {
+                        y[(size_t)mm * N + rows[h]] = v[h][j];
+                        if (ARGMAX)
+                            atomicMax(&ck[mm], argmax_key(v[h][j], rows[h]));
+                    }
+                }
+            }
+        }
+    } else {
+        float *red = reinterpret_cast<float *>(xs + 8 * cpr); // [rbc][ksplit][8][16]
+        float *r = red + (rbl * ksplit + ks) * 8 * 16;
+        r[m0 * 16 + g] = a0;
+        r[m1 * 16 + g] = a1;
+        r[m0 * 16 + g + 8] = b0;
+        r[m1 * 16 + g + 8] = b1;
+        __syncthreads();
+        for (int i = threadIdx.x; i < rbc * 8 * 16; i += blockDim.x) {
+            const int rr = i & 15, mm = (i >> 4) & 7, rl = i >> 7;
+            const int row = (blockIdx.x * rbc + rl) * 16 + rr;
+            float s = 0.f;
+            for (int k2 = 0; k2 < ksplit; ++k2)
+                s += red[((rl * ksplit + k2) * 8 + mm) * 16 + rr];
+            if (row < N && mm < M) {
+                y[(size_t)mm * N + row] = s;
+                if (ARGMAX)
+                    atomicMax(&ck[mm], argmax_key(s, row));
+            }
+        }
+    }
+    if (ARGMAX) {
+        __syncthreads();
+        if (threadIdx.x < M)
+            keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
+    }
+}
+
+// ---------------------------------------------------- argmax finalize ----
+
+__global__ void __launch_bounds__(256)
+argmax_finalize_kernel(int32_t *__restrict__ argmax, const unsigned long long *__restrict__ keys,
+                       int nblocks)
+{
+    pdl_wait();
+    const int m = blockIdx.x;
+    unsigned long long k = 0ull;
+    for (int i = threadIdx.x; i < nblocks; i += blockDim.x)
+        k = umax64(k, keys[(size_t)m * nblocks + i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        k = umax64(k, __shfl_xor_sync(0xFFFFFFFFu, k, o));
+    __shared__ unsigned long long wk[8];
+    if ((threadIdx.x & 31) == 0)
+        wk[threadIdx.x >> 5] = k;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned long long b = 0ull;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+            b = umax64(b, wk[w]);
+        argmax[m] = (int32_t)argmax_key_index(b);
+    }
+}
+
+// ------------------------------------------------------------- launch ----
+
+template <typename Kern, typename... Args>
+static cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename Kern>
+static cudaError_t set_smem(Kern kern, size_t bytes)
+{
+    if (bytes <= 48 * 1024)
+        return cudaSuccess;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+DecodePlan plan_decode(int M, int N, int K, int num_sms)
+{
+    DecodePlan p;
+    const int nrb = (N + 15) / 16;
+    if (M <= 2) {
+        const int T = (K + kTileK - 1) / kTileK;
+        const int target = num_sms * 12; // warps in flight for the weight stream
+        int ks = 1;
+        while (ks < 16 && (long long)nrb * ks < target && T >= 4 * ks)
+            ks *= 2;
+        p.kernel = 2;
+        p.ksplit = ks;
+        p.warps = ks >= 8 ? ks : 8;
+        p.unroll = 4;
+    } else {
+        const int ngroups = K / 32;
+        const int target = num_sms * 12;
+        int ks = 1;
+        while (ks < 16 && (long long)nrb * ks < target && ngroups >= 16 * ks)
+            ks *= 2;
+        p.kernel = 8;
+        p.ksplit = ks;
+        p.warps = ks >= 8 ? ks : 8;
+        p.unroll = 8;
+    }
+    const int rbc = p.warps / p.ksplit;
+    p.grid = (nrb + rbc - 1) / rbc;
+    return p;
+}
+
+template <int MX, bool ARGMAX>
+static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                             const uint16_t *sc, int N, int K, unsigned long long *keys,
+                             cudaStream_t s)
+{
+    const int Kpad = (K + kTileK - 1) / kTileK * kTileK;
+    const int rbc = p.warps / p.ksplit;
+    size_t smem = (size_t)MX * Kpad * 2 + 16;
+    if (p.ksplit > 1)
+        smem += (size_t)rbc * p.ksplit * MX * 16 * sizeof(float);
+    const bool sc32 = (K % 64) == 0;
+    auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, ARGMAX> : gemv_m2_kernel<MX, 4, false, ARGMAX>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(kern, dim3(p.grid), dim3(32 * p.warps), smem, s, y, x, qw, sc, N, K, p.ksplit,
+                      keys);
+}
+
+template <bool ARGMAX>
+static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                             const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
+                             cudaStream_t s)
+{
+    const int rbc = p.warps / p.ksplit;
+    size_t smem = (size_t)8 * K * 2;
+    if (p.ksplit > 1)
+        smem += (size_t)rbc * p.ksplit * 8 * 16 * sizeof(float);
+    auto kern = gemv_m8_kernel<8, ARGMAX>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(kern, dim3(p.grid), dim3(32 * p.warps), smem, s, y, x, qw, sc, M, N, K,
+                      p.ksplit, keys);
+}
+
+cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                       const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
+                       int32_t *argmax, cudaStream_t s)
+{
+    const bool am = argmax != nullptr;
+    cudaError_t e;
+    if (p.kernel == 2) {
+        if (M == 1)
+            e = am ? launch_m2<1, true>(p, y, x, qw, sc, N, K, keys, s)
+                   : launch_m2<1, false>(p, y, x, qw, sc, N, K, keys, s);
+        else
+            e = am ? launch_m2<2, true>(p, y, x, qw, sc, N, K, keys, s)
+                   : launch_m2<2, false>(p, y, x, qw, sc, N, K, keys, s);
+    } else {
+        e = am ? launch_m8<true>(p, y, x, qw, sc, M, N, K, keys, s)
+               : launch_m8<false>(p, y, x, qw, sc, M, N, K, keys, s);
+    }
+    if (e != cudaSuccess || !am)
+        return e;
+    return launch_pdl(argmax_finalize_kernel, dim3(M), dim3(256), 0, s, argmax,
+                      (const unsigned long long *)keys, p.grid);
+}
+
+} // namespace w4

@@ -1,0 +1,38 @@
+// Internal host-side interfaces between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+// Per-shape launch plan of the decode kernels (M <= 8).
+struct DecodePlan {
+    int kernel = 2; // 2: M <= 2 kernel (full-group 128-bit loads), 8: M <= 8 kernel
+    int ksplit = 1; // warps of a CTA that split K for one 16-row block
+    int warps = 8;  // warps per CTA
+    int unroll = 4; // k-tiles (m2) or groups (m8) in flight per warp
+    int grid = 1;
+};
+
+DecodePlan plan_decode(int M, int N, int K, int num_sms);
+
+// Launches the decode kernel (and, when argmax != nullptr, the argmax pass that
+// reduces keys[M][plan.grid]).
+cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                       const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
+                       int32_t *argmax, cudaStream_t s);
+
+cudaError_t run_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qt,
+                             const uint16_t *sc, int M, int N, int K, int32_t *status,
+                             cudaStream_t s);
+
+cudaError_t run_read_probe(unsigned long long *sum, const void *buf, size_t bytes, int num_sms,
+                           cudaStream_t s);
+
+// Prefill (M > 8) tensor-core GEMM.
+cudaError_t run_prefill(float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int M,
+                        int N, int K, int num_sms, cudaStream_t s);
+
+} // namespace w4

@@ -69,13 +69,19 @@ def uniform53(state0: int, start: int, count: int) -> np.ndarray:
     return (splitmix64(state0, start, count) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
 
 
-def normals(state0: int, count: int) -> np.ndarray:
-    """count N(0,1) values in fp64 by Box-Muller over consecutive draw pairs."""
+def normals(state0: int, count: int, start: int = 0) -> np.ndarray:
+    """N(0,1) values start .. start+count-1 of a Box-Muller stream (fp64).
+
+    Value 2j is r*cos(2*pi*u2) and value 2j+1 is r*sin(2*pi*u2) for the uniform
+    pair (draw 2j, draw 2j+1), r = sqrt(-2 ln(1 - draw 2j)). start must be even.
+    """
+    assert start % 2 == 0
     pairs = (count + 1) // 2
     out = np.empty(2 * pairs, dtype=np.float64)
+    p_base = start // 2
     for p0 in range(0, pairs, _CHUNK):
         n = min(_CHUNK, pairs - p0)
-        u = uniform53(state0, 2 * p0, 2 * n)
+        u = uniform53(state0, 2 * (p_base + p0), 2 * n)
         u1 = 1.0 - u[0::2]  # (0, 1], keeps log finite
         u2 = u[1::2]
         r = np.sqrt(-2.0 * np.log(u1))
@@ -112,6 +118,31 @@ def gen_scales(seed: int, n: int, k: int, group: int = 32) -> np.ndarray:
     return f64_to_bf16_bits(np.abs(z) * 0.02 + 1e-4).reshape(n, k // group)
 
 
+def gen_qweight_rows(seed: int, n: int, k: int, rows) -> np.ndarray:
+    """Rows `rows` of gen_qweight(seed, n, k) without drawing the whole table."""
+    w = k // 8
+    s = stream_state(seed, TAG_CODES)
+    out = np.empty((len(rows), w), dtype=np.uint32)
+    for i, r in enumerate(rows):
+        assert 0 <= r < n
+        out[i] = (splitmix64(s, int(r) * w, w) & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+    return out
+
+
+def gen_scales_rows(seed: int, n: int, k: int, rows, group: int = 32) -> np.ndarray:
+    """Rows `rows` of gen_scales(seed, n, k, group) without drawing the whole table."""
+    gpr = k // group
+    s = stream_state(seed, TAG_STEPS)
+    out = np.empty((len(rows), gpr), dtype=np.uint16)
+    for i, r in enumerate(rows):
+        assert 0 <= r < n
+        start = int(r) * gpr
+        lead = start % 2
+        z = normals(s, gpr + lead, start - lead)[lead:]
+        out[i] = f64_to_bf16_bits(np.abs(z) * 0.02 + 1e-4)
+    return out
+
+
 def gen_x(seed: int, m: int, k: int) -> np.ndarray:
     """bf16 bits [m][k], N(0,1). One row uses tag 2, several rows tag 4."""
     tag = TAG_X if m == 1 else TAG_XROWS
@@ -133,3 +164,47 @@ def gen_words(seed: int, nwords: int) -> np.ndarray:
 def gen_w4_problem(seed: int, m: int, n: int, k: int, group: int = 32):
     """(x bf16 [m][k], qweight u32 [n][k/8], scales bf16 [n][k/group]) for one projection."""
     return gen_x(seed, m, k), gen_qweight(seed, n, k), gen_scales(seed, n, k, group)
+
+
+# ---------------------------------------------------------------------------
+# Device-side copy of the integer streams (same bits as the numpy version).
+# Large code tables (GB) are drawn on the GPU with torch int64 arithmetic, which
+# wraps like uint64 for +, *, ^; the logical right shift is an arithmetic shift
+# followed by a mask. Only integer streams are drawn this way: the fp64
+# Box-Muller streams always come from numpy on the host.
+
+def _s64(v: int) -> int:
+    v &= 0xFFFFFFFFFFFFFFFF
+    return v - (1 << 64) if v >= (1 << 63) else v
+
+
+def splitmix64_torch(state0: int, start: int, count: int, device, chunk: int = 1 << 24):
+    import torch
+    out = torch.empty(count, dtype=torch.int64, device=device)
+    g, m1, m2, s0 = _s64(0x9E3779B97F4A7C15), _s64(0xBF58476D1CE4E5B9), _s64(0x94D049BB133111EB), _s64(state0)
+    for c0 in range(0, count, chunk):
+        n = min(chunk, count - c0)
+        z = torch.arange(start + c0 + 1, start + c0 + 1 + n, dtype=torch.int64, device=device)
+        z.mul_(g).add_(s0)
+        z.bitwise_xor_((z >> 30) & ((1 << 34) - 1))
+        z.mul_(m1)
+        z.bitwise_xor_((z >> 27) & ((1 << 37) - 1))
+        z.mul_(m2)
+        z.bitwise_xor_((z >> 31) & ((1 << 33) - 1))
+        out[c0:c0 + n] = z
+    return out
+
+
+def gen_qweight_torch(seed: int, n: int, k: int, device, out=None):
+    """Device int32 [n][k/8] with the same bits as gen_qweight(seed, n, k)."""
+    import torch
+    assert k % 8 == 0
+    count = n * (k // 8)
+    q = torch.empty(count, dtype=torch.int32, device=device) if out is None else out.view(-1)
+    chunk = 1 << 24
+    for c0 in range(0, count, chunk):
+        c = min(chunk, count - c0)
+        z = splitmix64_torch(stream_state(seed, TAG_CODES), c0, c, device)
+        lo = z & 0xFFFFFFFF
+        q[c0:c0 + c] = torch.where(lo >= (1 << 31), lo - (1 << 32), lo).to(torch.int32)
+    return q.view(n, k // 8)

@@ -1,0 +1,87 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every symbol
+the header declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_weight_only_w4a16_gb300 import build
+    path = build.build()
+    import bit_weight_only_w4a16_gb300 as w4
+    return w4._lib, path
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("w4a16_gemv", "w4a16_gemm", "w4a16_gemv_argmax", "w4_embed_gather", "hbm_read_probe",
+              "w4_init", "w4_status_string", "w4_last_cuda_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    l, path = lib
+    for n in _declared():
+        assert hasattr(l, n), n
+    import bit_weight_only_w4a16_gb300 as w4
+    assert set(w4.EXPORTS) <= set(_declared())
+
+
+def test_status_strings(lib):
+    l, _ = lib
+    assert l.w4_status_string(0) == b"W4_OK"
+    assert l.w4_status_string(3) == b"W4_ERR_MISALIGNED"
+    assert l.w4_status_string(99) == b"W4_ERR_UNKNOWN"
+
+
+def _addr(v):
+    return ctypes.c_void_p(v)
+
+
+def test_validation_before_any_launch(lib):
+    l, _ = lib
+    A = _addr(1 << 20)  # a 16-byte aligned non-NULL address; never dereferenced
+    # NULL pointer
+    assert l.w4a16_gemv(None, A, A, A, 1, 16, 64, 32, None) == 1
+    # sizes
+    assert l.w4a16_gemv(A, A, A, A, 0, 16, 64, 32, None) == 1
+    assert l.w4a16_gemv(A, A, A, A, 1, -1, 64, 32, None) == 1
+    assert l.w4a16_gemv(A, A, A, A, 1, 16, 48, 32, None) == 1
+    # group other than 32
+    assert l.w4a16_gemv(A, A, A, A, 1, 16, 128, 64, None) == 2
+    # M beyond the decode call
+    assert l.w4a16_gemv(A, A, A, A, 9, 16, 64, 32, None) == 2
+    assert l.w4a16_gemv_argmax(A, A, A, A, A, 9, 16, 64, 32, None) == 2
+    # misaligned
+    assert l.w4a16_gemv(A, _addr((1 << 20) + 2), A, A, 1, 16, 64, 32, None) == 3
+    assert l.w4a16_gemv(A, A, _addr((1 << 20) + 4), A, 1, 16, 64, 32, None) == 3
+    # index overflow
+    assert l.w4a16_gemv(A, A, A, A, 1, 1 << 30, 64, 32, None) == 1
+    # gather / probe
+    assert l.w4_embed_gather(A, A, A, A, 1, 10, 40, 32, None, None) == 1
+    assert l.w4_embed_gather(A, None, A, A, 1, 10, 64, 32, None, None) == 1
+    assert l.hbm_read_probe(A, A, ctypes.c_size_t(24), None) == 1
+    assert l.hbm_read_probe(A, _addr((1 << 20) + 8), ctypes.c_size_t(32), None) == 3
+    # prefill shape rules
+    assert l.w4a16_gemm(A, A, A, A, 64, 24, 64, 32, None) == 2
+    assert l.w4a16_gemm(A, A, A, A, 64, 32, 96, 32, None) == 2
+
+
+def test_no_device_reported_without_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    l, _ = lib
+    assert l.w4_init() == 5

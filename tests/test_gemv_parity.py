@@ -1,0 +1,192 @@
+"""GPU decode GEMV/GEMM (M <= 8) against the fp64 oracle, through the C ABI.
+
+Bar: |y - y_ref| <= 1e-4 * sum|w x| + 1e-6 elementwise; exact where the exact
+result is representable (hand examples, all-8 codes, power-of-two scaling);
+argmax index identical to the oracle's.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _util import assert_w4_close, to_dev_bits16, to_dev_u32
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def w4():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import bit_weight_only_w4a16_gb300 as w4
+    w4.init()
+    return w4
+
+
+def _run(w4, x, qw, sc, argmax=False):
+    import torch
+    xd, qd, sd = to_dev_bits16(x), to_dev_u32(qw), to_dev_bits16(sc)
+    if argmax:
+        y, a = w4.w4a16_gemv_argmax(xd, qd, sd)
+        torch.cuda.synchronize()
+        return y.cpu().numpy(), a.cpu().numpy()
+    y = w4.w4a16_gemm(xd, qd, sd)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def test_config0_full(w4):
+    # One W4A16 GEMV, M=1, N=K=2048, seed 0.
+    x, qw, sc = synth.gen_w4_problem(0, 1, 2048, 2048)
+    y = _run(w4, x, qw, sc)
+    yr, ar = oracle.gemm(x, qw, sc)
+    worst = assert_w4_close(y, yr, ar, what="config0")
+    assert worst < 1e-5
+
+
+def test_hand_worked_examples_exact(w4):
+    g = json.load(open(os.path.join(GOLDEN, "hand_2x64.json")))
+    rows = [g["rows"]["r0"], g["rows"]["r1"]]
+    qw = np.array([[int(w, 16) for w in r["words_hex"]] for r in rows], dtype=np.uint32)
+    sc = np.array([[int(s, 16) for s in r["steps_bf16_hex"]] for r in rows], dtype=np.uint16)
+    k = np.arange(64)
+    xs = {"ones": np.ones(64), "ramp": k.astype(float),
+          "alt": np.where(k % 2 == 0, 1.0, -1.0) * (1 + (k % 4) / 4)}
+    for case in g["cases"]:
+        x = synth.f64_to_bf16_bits(xs[case["x"]])[None, :]
+        y = _run(w4, x, qw, sc)
+        assert y[0].tolist() == case["y"], case["x"]
+    # M = 3 and M = 8 kernels on the same rows
+    x3 = np.stack([synth.f64_to_bf16_bits(xs[c]) for c in ("ones", "ramp", "alt")])
+    y3 = _run(w4, x3, qw, sc)
+    assert y3.tolist() == [c["y"] for c in g["cases"]]
+    x8 = np.concatenate([x3, x3, x3[:2]])
+    y8 = _run(w4, x8, qw, sc)
+    assert y8.tolist() == [c["y"] for c in g["cases"]] * 2 + [g["cases"][0]["y"], g["cases"][1]["y"]]
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 1, 32), (1, 17, 96), (1, 300, 160), (1, 33, 4192), (1, 64, 12288),
+    (2, 45, 2080), (2, 1, 64), (2, 1000, 416),
+    (3, 19, 64), (4, 1, 96), (5, 40, 224), (7, 300, 1056), (8, 16, 32), (8, 129, 1536),
+])
+def test_ragged_shapes(w4, M, N, K):
+    x, qw, sc = synth.gen_w4_problem(100 + M * 7 + N, M, N, K)
+    y = _run(w4, x, qw, sc)
+    yr, ar = oracle.gemm(x, qw, sc)
+    assert_w4_close(y, yr, ar, what=f"M{M} N{N} K{K}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 5, 8])
+def test_all_codes_eight_give_exact_zero(w4, M):
+    N, K = 70, 1536
+    qw = np.full((N, K // 8), 0x88888888, dtype=np.uint32)
+    sc = synth.gen_scales(5, N, K)
+    x = synth.gen_x(5, M, K)
+    y = _run(w4, x, qw, sc)
+    assert np.all(y == 0.0)
+
+
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_power_of_two_steps_scale_bit_exactly(w4, M):
+    x, qw, sc = synth.gen_w4_problem(41, M, 96, 2048)
+    y = _run(w4, x, qw, sc)
+    sc8 = (sc.astype(np.uint32) + (3 << 7)).astype(np.uint16)  # steps x 8
+    y8 = _run(w4, x, qw, sc8)
+    assert np.array_equal(y8, (8.0 * y).astype(np.float32))
+    yn = _run(w4, x ^ np.uint16(0x8000), qw, sc)
+    assert np.array_equal(yn, -y)
+
+
+def test_run_to_run_bitwise_identical(w4):
+    x, qw, sc = synth.gen_w4_problem(42, 1, 4096, 6144)
+    a = _run(w4, x, qw, sc)
+    b = _run(w4, x, qw, sc)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+# The decode weight sweep's matrix shapes (N x K), unfused and fused.
+SWEEP_SHAPES = [(2048, 1536), (256, 1536), (1536, 2048), (6144, 1536), (1536, 6144),
+                (12288, 1536), (1536, 12288), (2560, 1536), (24576, 1536)]
+
+
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("N,K", SWEEP_SHAPES)
+def test_sweep_shapes_sampled_rows(w4, M, N, K):
+    import torch
+    seed = 500 + N + K
+    x = synth.gen_x(seed, M, K)
+    qd = synth.gen_qweight_torch(seed, N, K, "cuda")
+    sc = synth.gen_scales(seed, N, K)
+    y = w4.w4a16_gemm(to_dev_bits16(x), qd, to_dev_bits16(sc))
+    torch.cuda.synchronize()
+    y = y.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 62)]))
+    qrows = synth.gen_qweight_rows(seed, N, K, rows)
+    yr, ar = oracle.gemm(x, qrows, sc[rows])
+    assert_w4_close(y[:, rows], yr, ar, what=f"sweep {N}x{K} M{M}")
+
+
+def test_device_qweight_generator_matches_host():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    a = synth.gen_qweight(9, 300, 1536)
+    b = synth.gen_qweight_torch(9, 300, 1536, "cuda").cpu().numpy().view(np.uint32)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("M", [1, 2, 8])
+def test_argmax_small(w4, M):
+    x, qw, sc = synth.gen_w4_problem(60 + M, M, 777, 1536)
+    y, a = _run(w4, x, qw, sc, argmax=True)
+    yr, ar = oracle.gemm(x, qw, sc)
+    assert_w4_close(y, yr, ar, what="argmax logits")
+    for m in range(M):
+        idx, gap = oracle.argmax(yr[m])
+        tol = 1e-4 * ar[m, idx] + 1e-6
+        assert gap > 2 * tol, "ambiguous seed"
+        assert a[m] == idx
+        assert a[m] == int(np.argmax(y[m]))
+
+
+def test_argmax_ties_pick_lowest_index(w4):
+    K, N = 1536, 200
+    x, qw, sc = synth.gen_w4_problem(70, 1, N, K)
+    yr, _ = oracle.gemm(x, qw, sc)
+    top = int(np.argmax(yr[0]))
+    for dup in (0, 17, top // 2):
+        q2, s2 = qw.copy(), sc.copy()
+        if dup == top:
+            continue
+        q2[dup], s2[dup] = qw[top], sc[top]
+        y, a = _run(w4, x, q2, s2, argmax=True)
+        first = int(np.flatnonzero(y[0] == y[0].max())[0])
+        assert a[0] == first
+        assert a[0] == min(dup, top)
+
+
+def test_vocab_projection_with_argmax(w4):
+    # N=262144 rows x K=1536, M=1, seed 1000: fp32 logits plus the fused greedy pick.
+    import torch
+    N, K, seed = 262144, 1536, 1000
+    x = synth.gen_x(seed, 1, K)
+    qd = synth.gen_qweight_torch(seed, N, K, "cuda")
+    sc = synth.gen_scales(seed, N, K)
+    y, a = w4.w4a16_gemv_argmax(to_dev_bits16(x), qd, to_dev_bits16(sc))
+    torch.cuda.synchronize()
+    y, a = y.cpu().numpy(), a.cpu().numpy()
+    qw = qd.cpu().numpy().view(np.uint32)
+    yr, ar = oracle.gemm(x, qw, sc)
+    assert_w4_close(y, yr, ar, what="vocab")
+    idx, gap = oracle.argmax(yr[0])
+    assert gap > 2 * (1e-4 * ar[0, idx] + 1e-6), "ambiguous seed"
+    assert int(a[0]) == idx
+    assert int(a[0]) == int(np.argmax(y[0]))
