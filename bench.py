@@ -237,8 +237,8 @@ def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
 
-    from bit_weight_only_w4a16_gb300 import build as _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import bit_weight_only_w4a16_gb300 as w4
 
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -12,9 +12,10 @@ HEADER = os.path.join(ROOT, "include", "w4a16.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from bit_weight_only_w4a16_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import bit_weight_only_w4a16_gb300 as w4
+    path = w4.LIB_PATH
     return w4._lib, path
 
 
