@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED",
                 3: "W4_ERR_MISALIGNED", 4: "W4_ERR_CUDA", 5: "W4_ERR_NO_DEVICE"}
 
 # Symbols declared in include/w4a16.h.
-EXPORTS = ("w4_status_string", "w4_last_cuda_error", "w4_init", "w4a16_gemv", "w4a16_gemm",
+EXPORTS = ("w4_status_string", "w4_last_cuda_error", "w4_init", "w4_device_error", "w4a16_gemv", "w4a16_gemm",
            "w4a16_gemv_argmax", "w4_embed_gather", "hbm_read_probe")
 
 
@@ -46,6 +46,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_last_cuda_error.restype = ctypes.c_char_p
     lib.w4_init.argtypes = []
     lib.w4_init.restype = I
+    lib.w4_device_error.argtypes = [P]
+    lib.w4_device_error.restype = I
     for name in ("w4a16_gemv", "w4a16_gemm"):
         f = getattr(lib, name)
         f.argtypes = [P, P, P, P, I, I, I, I, P]
@@ -102,6 +104,13 @@ def _u32(t, name):
 def init():
     """Set up the library on the current device (call before CUDA graph capture)."""
     _check(_lib.w4_init(), "w4_init")
+
+
+def device_error() -> int:
+    """Synchronize the device, then read and clear the library's device error word."""
+    code = ctypes.c_int32(0)
+    _check(_lib.w4_device_error(ctypes.byref(code)), "w4_device_error")
+    return int(code.value)
 
 
 def _shape(x, qweight, scales, group):

@@ -18,6 +18,7 @@ struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     unsigned long long *keys = nullptr;
+    int *err = nullptr; // device error word written by kernels whose bounded waits ran out
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -59,10 +60,14 @@ int device_state(DeviceState **out)
         if (major != 10 || minor != 3)
             return W4_ERR_NO_DEVICE; // kernels are built for sm_103a only
         void *p = nullptr;
-        e = cudaMalloc(&p, kKeyCapacity * sizeof(unsigned long long));
+        e = cudaMalloc(&p, kKeyCapacity * sizeof(unsigned long long) + 256);
         if (e != cudaSuccess)
             return cuda_fail(e);
         st.keys = static_cast<unsigned long long *>(p);
+        st.err = reinterpret_cast<int *>(static_cast<char *>(p) + kKeyCapacity * sizeof(unsigned long long));
+        e = cudaMemset(st.err, 0, sizeof(int));
+        if (e != cudaSuccess)
+            return cuda_fail(e);
         st.num_sms = sms;
         st.ready = true;
     }
@@ -140,11 +145,19 @@ int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (w4::stream_supported(M, N, K, qweight, scales)) {
+        const w4::StreamPlan sp = w4::plan_stream(M, N, K, st->num_sms);
+        if (sp.ok) {
+            cudaError_t e = w4::run_stream(sp, y, x, qweight, scales, M, N, K, nullptr, nullptr,
+                                           st->err, s);
+            return e == cudaSuccess ? W4_OK : cuda_fail(e);
+        }
+    }
     const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
     if (!decode_fits(p, M, K))
         return W4_ERR_UNSUPPORTED;
-    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, nullptr, nullptr,
-                                   static_cast<cudaStream_t>(stream));
+    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, nullptr, nullptr, s);
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 
@@ -183,11 +196,19 @@ int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (w4::stream_supported(M, N, K, qweight, scales)) {
+        const w4::StreamPlan sp = w4::plan_stream(M, N, K, st->num_sms);
+        if (sp.ok && (size_t)M * sp.C * sp.nclusters <= kKeyCapacity) {
+            cudaError_t e = w4::run_stream(sp, y, x, qweight, scales, M, N, K, st->keys, argmax,
+                                           st->err, s);
+            return e == cudaSuccess ? W4_OK : cuda_fail(e);
+        }
+    }
     const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
     if (!decode_fits(p, M, K) || (size_t)M * p.grid > kKeyCapacity)
         return W4_ERR_UNSUPPORTED;
-    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, st->keys, argmax,
-                                   static_cast<cudaStream_t>(stream));
+    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, st->keys, argmax, s);
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 
@@ -214,6 +235,22 @@ int w4_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qtable,
         return rc;
     cudaError_t e = w4::run_embed_gather(out, ids, qtable, scales, M, N, K, status,
                                          static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int w4_device_error(int32_t *code)
+{
+    if (!code)
+        return W4_ERR_INVALID_ARG;
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != W4_OK)
+        return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(code, st->err, sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess)
+        e = cudaMemset(st->err, 0, sizeof(int32_t));
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 

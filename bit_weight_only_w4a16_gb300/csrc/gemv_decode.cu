@@ -490,8 +490,13 @@ cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const u
     }
     if (e != cudaSuccess || !am)
         return e;
-    return launch_pdl(argmax_finalize_kernel, dim3(M), dim3(256), 0, s, argmax,
-                      (const unsigned long long *)keys, p.grid);
+    return run_argmax_finalize(argmax, keys, M, p.grid, s);
+}
+
+cudaError_t run_argmax_finalize(int32_t *argmax, const unsigned long long *keys, int M, int nblocks,
+                                cudaStream_t s)
+{
+    return launch_pdl(argmax_finalize_kernel, dim3(M), dim3(256), 0, s, argmax, keys, nblocks);
 }
 
 } // namespace w4

@@ -24,6 +24,24 @@ cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const u
                        const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
                        int32_t *argmax, cudaStream_t s);
 
+// Bulk-copy streaming decode kernel (M <= 2, K % 256 == 0, 16-byte aligned
+// codes and steps): cluster size C splits K, nclusters split the row blocks.
+struct StreamPlan {
+    int C = 1;
+    int nclusters = 1;
+    bool ok = false;
+};
+
+bool stream_supported(int M, int N, int K, const void *qw, const void *sc);
+StreamPlan plan_stream(int M, int N, int K, int num_sms);
+cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                       const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
+                       int32_t *argmax, int *err, cudaStream_t s);
+
+// argmax[m] = index of the largest key in keys[m][0 .. nblocks).
+cudaError_t run_argmax_finalize(int32_t *argmax, const unsigned long long *keys, int M, int nblocks,
+                                cudaStream_t s);
+
 cudaError_t run_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qt,
                              const uint16_t *sc, int M, int N, int K, int32_t *status,
                              cudaStream_t s);

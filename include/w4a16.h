@@ -55,11 +55,20 @@ const char *w4_last_cuda_error(void);
 
 /*
  * Set up the library on the current device: checks that it is sm_103 and
- * allocates the small library-owned scratch the argmax call uses (a few KB,
- * held until process exit). Idempotent. Call it before capturing any call of
- * this library in a CUDA graph; otherwise the first call on a device does it.
+ * allocates the library-owned device scratch (4 MB of argmax keys and one
+ * error word, held until process exit). Idempotent and thread-safe. Call it
+ * before capturing any call of this library in a CUDA graph; otherwise the
+ * first call on a device does it.
  */
 int w4_init(void);
+
+/*
+ * Reads and clears the device error word of the current device after a
+ * cudaDeviceSynchronize. *code is 0 when every kernel finished normally; bit 0
+ * means a kernel's bounded wait on its own shared-memory pipeline ran out (the
+ * kernel then returned without hanging, and its outputs are not valid).
+ */
+int w4_device_error(int32_t *code);
 
 /*
  * W4A16 matrix-vector product for decode, M in [1, 8].

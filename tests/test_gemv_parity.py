@@ -74,6 +74,9 @@ def test_hand_worked_examples_exact(w4):
 @pytest.mark.parametrize("M,N,K", [
     (1, 1, 32), (1, 17, 96), (1, 300, 160), (1, 33, 4192), (1, 64, 12288),
     (2, 45, 2080), (2, 1, 64), (2, 1000, 416),
+    # K % 256 == 0 with M <= 2 runs the bulk-copy streaming kernel
+    (1, 1, 256), (1, 17, 256), (2, 300, 512), (1, 33, 4352), (2, 777, 1536), (1, 70, 768),
+    (2, 96, 2048), (1, 4097, 6144),
     (3, 19, 64), (4, 1, 96), (5, 40, 224), (7, 300, 1056), (8, 16, 32), (8, 129, 1536),
 ])
 def test_ragged_shapes(w4, M, N, K):
@@ -190,3 +193,25 @@ def test_vocab_projection_with_argmax(w4):
     assert gap > 2 * (1e-4 * ar[0, idx] + 1e-6), "ambiguous seed"
     assert int(a[0]) == idx
     assert int(a[0]) == int(np.argmax(y[0]))
+
+
+def test_streaming_and_register_kernels_agree_with_oracle(w4):
+    # Scales that are 4- but not 16-byte aligned route K % 256 == 0 shapes to the
+    # register-streaming kernel; aligned ones to the bulk-copy kernel.
+    import torch
+    x, qw, sc = synth.gen_w4_problem(77, 1, 500, 1536)
+    yr, ar = oracle.gemm(x, qw, sc)
+    xd, qd = to_dev_bits16(x), to_dev_u32(qw)
+    flat = torch.zeros(sc.size + 8, dtype=torch.int16, device="cuda")
+    flat[2:2 + sc.size] = torch.from_numpy(sc.view(np.int16).ravel()).cuda()
+    sc_mis = flat[2:2 + sc.size].view(sc.shape)
+    sc_al = to_dev_bits16(sc)
+    assert sc_mis.data_ptr() % 16 != 0 and sc_al.data_ptr() % 16 == 0
+    for s_dev in (sc_al, sc_mis):
+        y = w4.w4a16_gemv(xd, qd, s_dev)
+        torch.cuda.synchronize()
+        assert_w4_close(y.cpu().numpy(), yr, ar, what="path")
+
+
+def test_no_device_error_reported(w4):
+    assert w4.device_error() == 0
