@@ -23,6 +23,9 @@
 // Work unit ("ku"): 16 rows x 256 k = 2 KB of codes + 256 B of steps. A stage
 // is up to `kus` consecutive ku of one row block, copied row by row into a
 // ring slot with a row pitch of 64 mod 128 bytes (conflict-free 128-bit reads).
+// Stage i belongs to consumer warp i % 8 and to one of that warp's own `dpw`
+// slots, so every slot's mbarrier phases are waited on in order by one warp
+// (a parity wait cannot tell phase u from phase u - 2).
 //
 // Inner product: the exact (code - 8) bf16 x bf16 m16n8k16 mma scheme of the
 // register-streaming decode kernel: lane (g, t) holds group 4*kt + t of rows g
@@ -35,7 +38,7 @@ namespace w4 {
 
 namespace {
 
-constexpr int kMaxSlots = 8;
+constexpr int kMaxSlots = 16;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
@@ -54,6 +57,7 @@ struct StreamArgs {
     int nclusters;  // row-block groups (one cluster each)
     int kus;        // max ku per stage
     int ns;         // ring slots in use (<= kMaxSlots)
+    int dpw;        // ring slots per consumer warp (1 or 2)
     int slot_bytes; // bytes per ring slot
     int pq, ps;     // smem row pitches of codes and steps inside a slot
     int off_x, off_spart, off_rbpart;
@@ -116,8 +120,9 @@ gemv_stream_kernel(const StreamArgs a)
         const uint64_t pol = policy_evict_first();
         const int row_words = a.K >> 3, row_steps = a.K >> 5;
         for (int i = 0; i < nst; ++i) {
-            const int slot = i % a.ns, use = i / a.ns;
-            if (i >= a.ns) {
+            const int slot = (i & (kConsumerWarps - 1)) + kConsumerWarps * ((i / kConsumerWarps) % a.dpw);
+            const int use = (i / kConsumerWarps) / a.dpw;
+            if (use > 0) {
                 int ok = 1;
                 if (lane == 0)
                     ok = mbar_wait_bounded(smem_addr(&empty_bar[slot]), (use - 1) & 1,
@@ -169,7 +174,8 @@ gemv_stream_kernel(const StreamArgs a)
         const int xstep = bsel ? 16 : 0, xi = bsel ? 1 : 0;
 
         for (int i = warp; i < nst; i += kConsumerWarps) {
-            const int slot = i % a.ns, use = i / a.ns;
+            const int slot = warp + kConsumerWarps * ((i / kConsumerWarps) % a.dpw);
+            const int use = (i / kConsumerWarps) / a.dpw;
             if (!mbar_wait_bounded(smem_addr(&full_bar[slot]), use & 1,
                                    s_abort ? kDrainLimit : kWaitLimit)) {
                 if (lane == 0) {
@@ -264,7 +270,7 @@ gemv_stream_kernel(const StreamArgs a)
 }
 
 struct Geometry {
-    int C = 1, nclusters = 1, kus = 1, ns = 1, slot_bytes = 0, pq = 0, ps = 0;
+    int C = 1, nclusters = 1, kus = 1, ns = 1, dpw = 1, slot_bytes = 0, pq = 0, ps = 0;
     int off_x = 0, off_spart = 0, off_rbpart = 0, smem = 0;
     bool ok = false;
 };
@@ -273,37 +279,51 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 Geometry make_geometry(int M, int N, int K, int C, int nclusters)
 {
+    // Among the stage sizes and slot counts that fit the budget, keep the one
+    // with the most bytes in flight (ties: larger stages).
     Geometry G;
+    long long best_inflight = -1;
     const int nrb = ceil_div(N, 16), nku = K / 256;
     G.C = C;
     G.nclusters = nclusters;
     const int nkuc_max = ceil_div(nku, C);
-    const int sprb = ceil_div(nkuc_max, 6);
-    G.kus = ceil_div(nkuc_max, sprb);
-    G.pq = G.kus * 128 + 64;
-    G.ps = G.kus * 16 + 16;
-    G.slot_bytes = 16 * G.pq + 16 * G.ps;
     const int rbc_max = ceil_div(nrb, nclusters);
-    const int max_stages = rbc_max * sprb;
     const int x_bytes = M * K * 2 + 16;
-    const int spart_bytes = max_stages * M * 16 * 4;
     const int rbpart_bytes = (C > 1) ? rbc_max * M * 16 * 4 : 0;
-    const int fixed = x_bytes + spart_bytes + rbpart_bytes;
-    const int fit = (kSmemBudget - fixed) / G.slot_bytes;
-    int ns = fit;
-    if (ns > kMaxSlots)
-        ns = kMaxSlots;
-    if (ns > max_stages)
-        ns = max_stages;
-    // Need double buffering unless every stage has its own slot.
-    if (ns < 1 || (fit < 2 && ns < max_stages))
-        return G;
-    G.ns = ns;
-    G.off_x = ns * G.slot_bytes;
-    G.off_spart = (G.off_x + x_bytes + 15) & ~15;
-    G.off_rbpart = (G.off_spart + spart_bytes + 15) & ~15;
-    G.smem = G.off_rbpart + rbpart_bytes;
-    G.ok = true;
+    for (int dpw = 2; dpw >= 1; --dpw) {
+        for (int kmax = 6; kmax >= 1; --kmax) {
+            const int sprb = ceil_div(nkuc_max, kmax);
+            const int kus = ceil_div(nkuc_max, sprb);
+            const int pq = kus * 128 + 64, ps = kus * 16 + 16;
+            const int slot_bytes = 16 * pq + 16 * ps;
+            const int max_stages = rbc_max * sprb;
+            const int spart_bytes = max_stages * M * 16 * 4;
+            int ns = kConsumerWarps * dpw;
+            if (ns > max_stages)
+                ns = max_stages;
+            const int off_x = ns * slot_bytes;
+            const int off_spart = (off_x + x_bytes + 15) & ~15;
+            const int off_rbpart = (off_spart + spart_bytes + 15) & ~15;
+            const int total = off_rbpart + rbpart_bytes;
+            if (total > kSmemBudget)
+                continue;
+            const long long inflight = (long long)ns * slot_bytes;
+            if (inflight <= best_inflight)
+                continue;
+            best_inflight = inflight;
+            G.kus = kus;
+            G.pq = pq;
+            G.ps = ps;
+            G.slot_bytes = slot_bytes;
+            G.ns = ns;
+            G.dpw = dpw;
+            G.off_x = off_x;
+            G.off_spart = off_spart;
+            G.off_rbpart = off_rbpart;
+            G.smem = total;
+            G.ok = true;
+        }
+    }
     return G;
 }
 
@@ -389,6 +409,7 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
     a.nclusters = G.nclusters;
     a.kus = G.kus;
     a.ns = G.ns;
+    a.dpw = G.dpw;
     a.slot_bytes = G.slot_bytes;
     a.pq = G.pq;
     a.ps = G.ps;
