@@ -1,4 +1,4 @@
-// Decode W4A16 GEMV (M = 1 or 2) with bulk-copy weight streaming.
+// Decode W4A16 GEMV (M = 1 or 2) with TMA-streamed weights.
 //
 // Source: "Gemma 4 E2B on a 4 GB GPU with pure PyTorch" - the w4gemv paragraph
 // (decode reads every weight once, straight from the packed 4-bit words, and
@@ -7,32 +7,40 @@
 // hundreds of small kernels replayed as one graph).
 //
 // Why this shape on GB300. A decode step is a chain of dependent GEMVs of
-// 0.25-3 us of HBM time each, and a dependent kernel boundary costs ~0.9 us even
-// under programmatic dependent launch. So each kernel:
-//   1. starts streaming its whole weight share into shared memory at once
-//      (1-D bulk copies issued by one producer warp, completion on mbarriers),
-//      before waiting on the previous kernel (griddepcontrol.wait), so the
-//      stream overlaps the previous kernel and the launch gap;
+// 0.25-3 us of HBM time each, a dependent kernel boundary costs ~0.9 us even
+// under programmatic dependent launch, and HBM needs ~100 KB in flight per SM.
+// So each kernel:
+//   1. starts streaming its weight share into a shared-memory ring at once with
+//      3-D tensor copies (one op per stage: 16 rows x kus x 256 k of codes, and
+//      one for their steps), issued by a producer warp before the kernel waits
+//      on the previous one (griddepcontrol.wait); the stream overlaps the
+//      previous kernel and the launch gap;
 //   2. keeps every SM busy after the wait: rows are split across clusters in
 //      whole 16-row blocks and K is split across the CTAs of a cluster, whose
 //      partial sums are added through distributed shared memory in a fixed
-//      rank order (deterministic, no global scratch, no atomics on y);
+//      rank order (deterministic; no global scratch; no atomics on y);
 //   3. stays under half of an SM's shared memory so the next kernel's CTAs can
 //      be resident at the same time and stream their weights.
 //
-// Work unit ("ku"): 16 rows x 256 k = 2 KB of codes + 256 B of steps. A stage
-// is up to `kus` consecutive ku of one row block, copied row by row into a
-// ring slot with a row pitch of 64 mod 128 bytes (conflict-free 128-bit reads).
+// Layout in shared memory. Codes arrive as [row][ku][128 B] with the hardware's
+// 128-byte swizzle (16-byte chunk c of line L lands at chunk c ^ (L & 7)); the
+// mma row -> weight row map pairs rows whose lines differ in bit 2 of L & 7, so
+// every 8-lane phase of a 128-bit read touches all 32 banks once. Steps arrive
+// as [row][ku][8 x bf16] without swizzle.
 // Stage i belongs to consumer warp i % 8 and to one of that warp's own `dpw`
-// slots, so every slot's mbarrier phases are waited on in order by one warp
-// (a parity wait cannot tell phase u from phase u - 2).
+// slots, so each slot's mbarrier phases are waited on in order by one warp.
 //
-// Inner product: the exact (code - 8) bf16 x bf16 m16n8k16 mma scheme of the
-// register-streaming decode kernel: lane (g, t) holds group 4*kt + t of rows g
-// and g+8; B column 4*m + s carries x-row m on group slot s; the group step is
-// applied in fp32 per (row, group).
+// Inner product: exact (code - 8) bf16 x bf16 m16n8k16 mma with fp32 accumulate.
+// Lane (g, t) holds group 4*kt + t of two weight rows; B column 4*m + s carries
+// x-row m on group slot s (zero elsewhere), so C[row][4m+s] is the unscaled
+// partial of one (row, group, x-row), scaled by its step in fp32.
 #include "common.cuh"
 #include "internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 namespace w4 {
 
@@ -49,21 +57,32 @@ constexpr int kSmemBudget = 110 * 1024;
 struct StreamArgs {
     float *y;
     const uint16_t *x;
-    const uint32_t *qw;
-    const uint16_t *sc;
     unsigned long long *keys; // argmax keys [MX][gridDim.x] or null
     int *err;                 // device error word (bit 0: a wait timed out)
     int N, K;
-    int nclusters;  // row-block groups (one cluster each)
-    int kus;        // max ku per stage
-    int ns;         // ring slots in use (<= kMaxSlots)
-    int dpw;        // ring slots per consumer warp (1 or 2)
-    int slot_bytes; // bytes per ring slot
-    int pq, ps;     // smem row pitches of codes and steps inside a slot
+    int nclusters;   // row-block groups (one cluster each)
+    int kus;         // ku (256-k units) per stage
+    int ns;          // ring slots in use (<= kMaxSlots)
+    int dpw;         // ring slots per consumer warp (1 or 2)
+    int off_steps;   // offset of the steps ring (codes ring at the aligned base)
     int off_x, off_spart, off_rbpart;
+    uint32_t perm_lo, perm_hi; // mma row g -> weight row, 4 bits each (g < 8, g >= 8)
 };
 
-template <int MX>
+struct StreamMaps {
+    CUtensorMap codes; // uint32 {32, K/256, N}, box {32, kus, 16}, 128-byte swizzle
+    CUtensorMap steps; // uint16 {8, K/256, N},  box {8, kus, 16}
+};
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+                 "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void emit(const StreamArgs &a, int m, int row, float v,
                                      unsigned long long *s_key, bool argmax)
 {
@@ -76,13 +95,16 @@ __device__ __forceinline__ void emit(const StreamArgs &a, int m, int row, float 
 
 template <int MX, bool ARGMAX>
 __global__ void __launch_bounds__(kThreads, 2)
-gemv_stream_kernel(const StreamArgs a)
+gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 {
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) unsigned long long full_bar[kMaxSlots];
     __shared__ __align__(8) unsigned long long empty_bar[kMaxSlots];
     __shared__ int s_abort;
     __shared__ unsigned long long s_key[MX];
+
+    // Codes ring on a 1024-byte boundary (the swizzle pattern's period).
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int C = (int)(gridDim.x / a.nclusters);
@@ -92,10 +114,10 @@ gemv_stream_kernel(const StreamArgs a)
     const int nku = a.K >> 8;
     const int rb0 = (int)((long long)cid * nrb / a.nclusters);
     const int nrbc = (int)((long long)(cid + 1) * nrb / a.nclusters) - rb0;
-    const int ku0 = (int)((long long)crank * nku / C);
-    const int nkuc = (int)((long long)(crank + 1) * nku / C) - ku0;
-    const int sprb = (nkuc + a.kus - 1) / a.kus; // stages per row block
+    const int ku0 = crank * (nku / C);  // C divides nku
+    const int sprb = (nku / C) / a.kus; // stages per row block; kus divides nku / C
     const int nst = nrbc * sprb;
+    const int code_slot = a.kus * 2048, step_slot = a.kus * 256;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.ns; ++i) {
@@ -110,48 +132,32 @@ gemv_stream_kernel(const StreamArgs a)
     __syncthreads();
     pdl_launch_dependents();
 
-    const uint32_t ring = smem_addr(smem);
+    const uint32_t codes_ring = smem_addr(smem);
+    const uint32_t steps_ring = codes_ring + a.off_steps;
     float *spart = reinterpret_cast<float *>(smem + a.off_spart);
     float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart);
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------- producer warp
         // Weights do not depend on earlier kernels, so no griddepcontrol.wait.
-        const uint64_t pol = policy_evict_first();
-        const int row_words = a.K >> 3, row_steps = a.K >> 5;
-        for (int i = 0; i < nst; ++i) {
-            const int slot = (i & (kConsumerWarps - 1)) + kConsumerWarps * ((i / kConsumerWarps) % a.dpw);
-            const int use = (i / kConsumerWarps) / a.dpw;
-            if (use > 0) {
-                int ok = 1;
-                if (lane == 0)
-                    ok = mbar_wait_bounded(smem_addr(&empty_bar[slot]), (use - 1) & 1,
-                                           s_abort ? kDrainLimit : kWaitLimit);
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok && lane == 0) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            const uint32_t tx = (uint32_t)(code_slot + step_slot);
+            for (int i = 0; i < nst; ++i) {
+                const int slot = (i % kConsumerWarps) + kConsumerWarps * ((i / kConsumerWarps) % a.dpw);
+                const int use = (i / kConsumerWarps) / a.dpw;
+                if (use > 0 && !mbar_wait_bounded(smem_addr(&empty_bar[slot]), (use - 1) & 1,
+                                                  s_abort ? kDrainLimit : kWaitLimit)) {
                     s_abort = 1;
                     atomicOr(a.err, 1);
                 }
-            }
-            const int rbl = i / sprb, j = i - rbl * sprb;
-            const int rb = rb0 + rbl;
-            const int kua = ku0 + j * a.kus;
-            const int nk = min(a.kus, ku0 + nkuc - kua);
-            const int rows = min(16, a.N - rb * 16);
-            const uint32_t qbytes = nk * 128u, sbytes = nk * 16u;
-            const uint32_t bar = smem_addr(&full_bar[slot]);
-            if (lane == 0)
-                mbar_arrive_expect_tx(bar, rows * (qbytes + sbytes));
-            __syncwarp();
-            const uint32_t sb = ring + slot * a.slot_bytes;
-            const int r = lane & 15;
-            if (r < rows) {
-                const size_t row = (size_t)rb * 16 + r;
-                if (lane < 16)
-                    bulk_g2s(sb + r * a.pq, a.qw + row * row_words + kua * 32, qbytes, bar, pol);
-                else
-                    bulk_g2s(sb + 16 * a.pq + r * a.ps, a.sc + row * row_steps + kua * 8, sbytes, bar,
-                             pol);
+                const int rbl = i / sprb, j = i - rbl * sprb;
+                const int rb = rb0 + rbl;
+                const int kua = ku0 + j * a.kus;
+                const uint32_t bar = smem_addr(&full_bar[slot]);
+                mbar_arrive_expect_tx(bar, tx);
+                tma_load_3d(codes_ring + slot * code_slot, &maps.codes, 0, kua, rb * 16, bar, pol);
+                tma_load_3d(steps_ring + slot * step_slot, &maps.steps, 0, kua, rb * 16, bar, pol);
             }
         }
     } else {
@@ -172,6 +178,8 @@ gemv_stream_kernel(const StreamArgs a)
         const bool bsel = ((g & 3) == t) && (bm < MX);
         const uint4 *xrow = bsel ? xs + bm * cpr + 4 * t : xs + MX * cpr;
         const int xstep = bsel ? 16 : 0, xi = bsel ? 1 : 0;
+        const int ra = (int)((a.perm_lo >> (4 * g)) & 15u);  // weight row of mma row g
+        const int rbr = (int)((a.perm_hi >> (4 * g)) & 15u); // weight row of mma row g + 8
 
         for (int i = warp; i < nst; i += kConsumerWarps) {
             const int slot = warp + kConsumerWarps * ((i / kConsumerWarps) % a.dpw);
@@ -185,20 +193,23 @@ gemv_stream_kernel(const StreamArgs a)
             }
             const int rbl = i / sprb, j = i - rbl * sprb;
             const int kua = ku0 + j * a.kus;
-            const int nk = min(a.kus, ku0 + nkuc - kua);
-            const unsigned char *sbp = smem + slot * a.slot_bytes;
-            const unsigned char *qa = sbp + g * a.pq + t * 16;
-            const unsigned char *qb = qa + 8 * a.pq;
-            const unsigned char *pa = sbp + 16 * a.pq + g * a.ps + 4 * (t & 1);
-            const unsigned char *pb = pa + 8 * a.ps;
+            const unsigned char *cb = smem + slot * code_slot;
+            const unsigned char *sb = smem + a.off_steps + slot * step_slot;
+            const int la0 = ra * a.kus, lb0 = rbr * a.kus; // first 128-byte line of each row
+            const unsigned char *pa = sb + la0 * 16 + 4 * (t & 1);
+            const unsigned char *pb = sb + lb0 * 16 + 4 * (t & 1);
             const uint4 *xb0 = xrow + xstep * (2 * kua);
             float accA = 0.f, accB = 0.f;
 #pragma unroll 2
-            for (int kt = 0; kt < 2 * nk; ++kt) {
-                const uint4 wa = *reinterpret_cast<const uint4 *>(qa + kt * 64);
-                const uint4 wb = *reinterpret_cast<const uint4 *>(qb + kt * 64);
-                const uint32_t sa = *reinterpret_cast<const uint32_t *>(pa + kt * 8);
-                const uint32_t sbv = *reinterpret_cast<const uint32_t *>(pb + kt * 8);
+            for (int kt = 0; kt < 2 * a.kus; ++kt) {
+                const int u = kt >> 1, ch = 4 * (kt & 1) + t;
+                const int la = la0 + u, lb = lb0 + u;
+                const uint4 wa =
+                    *reinterpret_cast<const uint4 *>(cb + la * 128 + ((ch ^ (la & 7)) << 4));
+                const uint4 wb =
+                    *reinterpret_cast<const uint4 *>(cb + lb * 128 + ((ch ^ (lb & 7)) << 4));
+                const uint32_t sa = *reinterpret_cast<const uint32_t *>(pa + u * 16 + 8 * (kt & 1));
+                const uint32_t sbv = *reinterpret_cast<const uint32_t *>(pb + u * 16 + 8 * (kt & 1));
                 const uint4 *xb = xb0 + xstep * kt;
                 const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w};
                 const uint32_t bw[4] = {wb.x, wb.y, wb.z, wb.w};
@@ -224,8 +235,8 @@ gemv_stream_kernel(const StreamArgs a)
             accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
             const int m = t >> 1;
             if ((t & 1) == 0 && m < MX) {
-                spart[(i * MX + m) * 16 + g] = accA;
-                spart[(i * MX + m) * 16 + g + 8] = accB;
+                spart[(i * MX + m) * 16 + ra] = accA;
+                spart[(i * MX + m) * 16 + rbr] = accB;
             }
         }
         named_sync(1, kConsumers);
@@ -237,7 +248,7 @@ gemv_stream_kernel(const StreamArgs a)
             for (int j = 0; j < sprb; ++j)
                 s += spart[((rbl * sprb + j) * MX + m) * 16 + rr];
             if (C == 1)
-                emit<MX>(a, m, (rb0 + rbl) * 16 + rr, s, s_key, ARGMAX);
+                emit(a, m, (rb0 + rbl) * 16 + rr, s, s_key, ARGMAX);
             else
                 rbpart[e] = s;
         }
@@ -256,7 +267,7 @@ gemv_stream_kernel(const StreamArgs a)
                 for (int c = 0; c < C; ++c)
                     s += ld_cluster_f32(map_rank(base + 4u * e, (uint32_t)c));
                 const int rr = e & 15, m = (e >> 4) % MX, rbl = e / (16 * MX);
-                emit<MX>(a, m, (rb0 + rbl) * 16 + rr, s, s_key, ARGMAX);
+                emit(a, m, (rb0 + rbl) * 16 + rr, s, s_key, ARGMAX);
             }
         }
         cluster_sync(); // no CTA leaves while another still reads its shared memory
@@ -269,66 +280,136 @@ gemv_stream_kernel(const StreamArgs a)
     }
 }
 
-struct Geometry {
-    int C = 1, nclusters = 1, kus = 1, ns = 1, dpw = 1, slot_bytes = 0, pq = 0, ps = 0;
-    int off_x = 0, off_spart = 0, off_rbpart = 0, smem = 0;
-    bool ok = false;
-};
+// ------------------------------------------------------------ host side ----
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Largest divisor of n that is <= cap.
+int divisor_at_most(int n, int cap)
+{
+    for (int d = cap; d >= 1; --d)
+        if (n % d == 0)
+            return d;
+    return 1;
+}
+
+struct Geometry {
+    int C = 1, nclusters = 1, kus = 1, ns = 1, dpw = 1;
+    int off_steps = 0, off_x = 0, off_spart = 0, off_rbpart = 0, smem = 0;
+    bool ok = false;
+};
+
 Geometry make_geometry(int M, int N, int K, int C, int nclusters)
 {
-    // Among the stage sizes and slot counts that fit the budget, keep the one
-    // with the most bytes in flight (ties: larger stages).
     Geometry G;
-    long long best_inflight = -1;
     const int nrb = ceil_div(N, 16), nku = K / 256;
+    if (nku % C != 0)
+        return G;
+    const int nkuc = nku / C;
     G.C = C;
     G.nclusters = nclusters;
-    const int nkuc_max = ceil_div(nku, C);
+    G.kus = divisor_at_most(nkuc, 6);
+    const int sprb = nkuc / G.kus;
     const int rbc_max = ceil_div(nrb, nclusters);
+    const int max_stages = rbc_max * sprb;
+    const int code_slot = G.kus * 2048, step_slot = G.kus * 256;
     const int x_bytes = M * K * 2 + 16;
+    const int spart_bytes = max_stages * M * 16 * 4;
     const int rbpart_bytes = (C > 1) ? rbc_max * M * 16 * 4 : 0;
     for (int dpw = 2; dpw >= 1; --dpw) {
-        for (int kmax = 6; kmax >= 1; --kmax) {
-            const int sprb = ceil_div(nkuc_max, kmax);
-            const int kus = ceil_div(nkuc_max, sprb);
-            const int pq = kus * 128 + 64, ps = kus * 16 + 16;
-            const int slot_bytes = 16 * pq + 16 * ps;
-            const int max_stages = rbc_max * sprb;
-            const int spart_bytes = max_stages * M * 16 * 4;
-            int ns = kConsumerWarps * dpw;
-            if (ns > max_stages)
-                ns = max_stages;
-            const int off_x = ns * slot_bytes;
-            const int off_spart = (off_x + x_bytes + 15) & ~15;
-            const int off_rbpart = (off_spart + spart_bytes + 15) & ~15;
-            const int total = off_rbpart + rbpart_bytes;
-            if (total > kSmemBudget)
-                continue;
-            const long long inflight = (long long)ns * slot_bytes;
-            if (inflight <= best_inflight)
-                continue;
-            best_inflight = inflight;
-            G.kus = kus;
-            G.pq = pq;
-            G.ps = ps;
-            G.slot_bytes = slot_bytes;
-            G.ns = ns;
-            G.dpw = dpw;
-            G.off_x = off_x;
-            G.off_spart = off_spart;
-            G.off_rbpart = off_rbpart;
-            G.smem = total;
-            G.ok = true;
-        }
+        int ns = kConsumerWarps * dpw;
+        if (ns > max_stages)
+            ns = max_stages;
+        const int off_steps = ns * code_slot;
+        const int off_x = (off_steps + ns * step_slot + 15) & ~15;
+        const int off_spart = (off_x + x_bytes + 15) & ~15;
+        const int off_rbpart = (off_spart + spart_bytes + 15) & ~15;
+        const int total = off_rbpart + rbpart_bytes + 1024; // + alignment slack
+        if (total > kSmemBudget)
+            continue;
+        G.ns = ns;
+        G.dpw = dpw;
+        G.off_steps = off_steps;
+        G.off_x = off_x;
+        G.off_spart = off_spart;
+        G.off_rbpart = off_rbpart;
+        G.smem = total;
+        G.ok = true;
+        return G;
     }
     return G;
 }
 
+// mma row -> weight row map that keeps 128-bit reads of the swizzled codes
+// conflict-free: the two rows read by one 8-lane phase differ in bit 2 of
+// (row * kus + u) & 7 for every u < kus (pairs r, r+4 for odd kus; r, r+2 for
+// kus = 2 mod 4; r, r+1 for kus = 0 mod 4).
+void row_perm(int kus, uint32_t &lo, uint32_t &hi)
+{
+    int p[16];
+    const int d = (kus & 1) ? 4 : ((kus & 3) == 2 ? 2 : 1);
+    for (int h = 0; h < 2; ++h) {
+        int n = 0;
+        for (int r = 0; r < 8 && n < 8; ++r) {
+            if ((r / d) % 2 == 0) {
+                p[8 * h + n++] = 8 * h + r;
+                p[8 * h + n++] = 8 * h + r + d;
+            }
+        }
+    }
+    lo = hi = 0;
+    for (int g = 0; g < 8; ++g) {
+        lo |= (uint32_t)p[g] << (4 * g);
+        hi |= (uint32_t)p[8 + g] << (4 * g);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, int K, int kus)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const cuuint64_t nku = (cuuint64_t)(K / 256);
+    cuuint32_t es[3] = {1, 1, 1};
+    {
+        cuuint64_t dims[3] = {32, nku, (cuuint64_t)N};
+        cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
+        cuuint32_t box[3] = {32, (cuuint32_t)kus, 16};
+        if (enc(&m.codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        cuuint64_t dims[3] = {8, nku, (cuuint64_t)N};
+        cuuint64_t strides[2] = {16, (cuuint64_t)K / 16};
+        cuuint32_t box[3] = {8, (cuuint32_t)kus, 16};
+        if (enc(&m.steps, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t *>(sc), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
 template <int MX, bool ARGMAX>
-cudaError_t launch_stream(const Geometry &G, const StreamArgs &a, cudaStream_t s)
+cudaError_t launch_stream(const Geometry &G, const StreamArgs &a, const StreamMaps &maps,
+                          cudaStream_t s)
 {
     auto kern = gemv_stream_kernel<MX, ARGMAX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G.smem);
@@ -348,7 +429,7 @@ cudaError_t launch_stream(const Geometry &G, const StreamArgs &a, cudaStream_t s
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, a, maps);
 }
 
 } // namespace
@@ -357,36 +438,38 @@ bool stream_supported(int M, int N, int K, const void *qw, const void *sc)
 {
     (void)N;
     return M >= 1 && M <= 2 && K % 256 == 0 && (reinterpret_cast<uintptr_t>(qw) & 15) == 0 &&
-           (reinterpret_cast<uintptr_t>(sc) & 15) == 0;
+           (reinterpret_cast<uintptr_t>(sc) & 15) == 0 && tensor_map_encoder() != nullptr;
 }
 
 StreamPlan plan_stream(int M, int N, int K, int num_sms)
 {
-    // Per-shape tiling: pick the cluster size C (K slices) and the number of
-    // clusters that minimise the largest per-CTA share, one CTA per SM.
+    // Per-shape tiling: the cluster size C (K slices, C | K/256) and the number
+    // of clusters that minimise the largest per-CTA share, one CTA per SM;
+    // smaller tensor copies cost more per byte, so the share is weighted by
+    // (1 + 1/kus).
     StreamPlan best;
     const int nrb = ceil_div(N, 16), nku = K / 256;
-    long long best_work = -1;
+    double best_cost = -1.0;
     const int cands[] = {1, 2, 3, 4, 6, 8};
     for (int C : cands) {
-        if (C > nku)
+        if (nku % C != 0)
             continue;
         int ncl = num_sms / C;
         if (ncl > nrb)
             ncl = nrb;
         if (ncl < 1)
             continue;
-        const long long work = (long long)ceil_div(nrb, ncl) * ceil_div(nku, C);
         const Geometry G = make_geometry(M, N, K, C, ncl);
         if (!G.ok)
             continue;
-        if (best_work < 0 || work < best_work) {
-            best_work = work;
+        const double cost = (double)ceil_div(nrb, ncl) * (nku / C) * (1.0 + 1.0 / G.kus);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
             best.C = C;
             best.nclusters = ncl;
         }
     }
-    best.ok = best_work >= 0;
+    best.ok = best_cost >= 0;
     return best;
 }
 
@@ -397,11 +480,12 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
     const Geometry G = make_geometry(M, N, K, p.C, p.nclusters);
     if (!G.ok)
         return cudaErrorInvalidConfiguration;
+    StreamMaps maps;
+    if (!encode_maps(maps, qw, sc, N, K, G.kus))
+        return cudaErrorInvalidValue;
     StreamArgs a;
     a.y = y;
     a.x = x;
-    a.qw = qw;
-    a.sc = sc;
     a.keys = keys;
     a.err = err;
     a.N = N;
@@ -410,18 +494,17 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
     a.kus = G.kus;
     a.ns = G.ns;
     a.dpw = G.dpw;
-    a.slot_bytes = G.slot_bytes;
-    a.pq = G.pq;
-    a.ps = G.ps;
+    a.off_steps = G.off_steps;
     a.off_x = G.off_x;
     a.off_spart = G.off_spart;
     a.off_rbpart = G.off_rbpart;
+    row_perm(G.kus, a.perm_lo, a.perm_hi);
     const bool am = argmax != nullptr;
     cudaError_t e;
     if (M == 1)
-        e = am ? launch_stream<1, true>(G, a, s) : launch_stream<1, false>(G, a, s);
+        e = am ? launch_stream<1, true>(G, a, maps, s) : launch_stream<1, false>(G, a, maps, s);
     else
-        e = am ? launch_stream<2, true>(G, a, s) : launch_stream<2, false>(G, a, s);
+        e = am ? launch_stream<2, true>(G, a, maps, s) : launch_stream<2, false>(G, a, maps, s);
     if (e != cudaSuccess || !am)
         return e;
     return run_argmax_finalize(argmax, keys, M, G.C * G.nclusters, s);
