@@ -11,24 +11,25 @@
 // under programmatic dependent launch, and HBM needs ~100 KB in flight per SM.
 // So each kernel:
 //   1. starts streaming its weight share into a shared-memory ring at once with
-//      3-D tensor copies (one op per stage: 16 rows x kus x 256 k of codes, and
+//      3-D tensor copies (one op per stage: 64 rows x kus x 256 k of codes, and
 //      one for their steps), issued by a producer warp before the kernel waits
 //      on the previous one (griddepcontrol.wait); the stream overlaps the
 //      previous kernel and the launch gap;
 //   2. keeps every SM busy after the wait: rows are split across clusters in
-//      whole 16-row blocks and K is split across the CTAs of a cluster, whose
+//      whole 64-row groups and K is split across the CTAs of a cluster, whose
 //      partial sums are added through distributed shared memory in a fixed
 //      rank order (deterministic; no global scratch; no atomics on y);
 //   3. stays under half of an SM's shared memory so the next kernel's CTAs can
 //      be resident at the same time and stream their weights.
 //
-// Layout in shared memory. Codes arrive as [row][ku][128 B] with the hardware's
-// 128-byte swizzle (16-byte chunk c of line L lands at chunk c ^ (L & 7)); the
-// mma row -> weight row map pairs rows whose lines differ in bit 2 of L & 7, so
-// every 8-lane phase of a 128-bit read touches all 32 banks once. Steps arrive
-// as [row][ku][8 x bf16] without swizzle.
-// Stage i belongs to consumer warp i % 8 and to one of that warp's own `dpw`
-// slots, so each slot's mbarrier phases are waited on in order by one warp.
+// Stages. A stage is 64 rows (4 row blocks) x kus ku of one CTA's K slice; all
+// 8 consumer warps read every stage (warp w: row block w & 3, k-tile half
+// w >> 2), so stages are consumed and their slots refilled in order and the
+// whole ring stays in flight. Codes arrive as [row][ku][128 B] with the
+// hardware's 128-byte swizzle (16-byte chunk c of line L lands at chunk
+// c ^ (L & 7)); the mma row -> weight row map pairs rows whose lines differ in
+// bit 2 of L & 7, so every 8-lane phase of a 128-bit read touches all 32 banks
+// once. Steps arrive as [row][ku][8 x bf16] without swizzle.
 //
 // Inner product: exact (code - 8) bf16 x bf16 m16n8k16 mma with fp32 accumulate.
 // Lane (g, t) holds group 4*kt + t of two weight rows; B column 4*m + s carries
@@ -50,6 +51,7 @@ constexpr int kMaxSlots = 16;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
+constexpr int kGroupRows = 64;       // rows per stage (4 row blocks of 16)
 constexpr int kWaitLimit = 1 << 22;  // polls before a wait is declared failed
 constexpr int kDrainLimit = 1 << 10; // polls per wait once a failure was seen
 constexpr int kSmemBudget = 110 * 1024;
@@ -60,18 +62,17 @@ struct StreamArgs {
     unsigned long long *keys; // argmax keys [MX][gridDim.x] or null
     int *err;                 // device error word (bit 0: a wait timed out)
     int N, K;
-    int nclusters;   // row-block groups (one cluster each)
+    int nclusters;   // row-group ranges (one cluster each)
     int kus;         // ku (256-k units) per stage
-    int ns;          // ring slots in use (<= kMaxSlots)
-    int dpw;         // ring slots per consumer warp (1 or 2)
+    int ns;          // ring slots
     int off_steps;   // offset of the steps ring (codes ring at the aligned base)
     int off_x, off_spart, off_rbpart;
-    uint32_t perm_lo, perm_hi; // mma row g -> weight row, 4 bits each (g < 8, g >= 8)
+    uint32_t perm_lo, perm_hi; // mma row g -> row of the block, 4 bits each (g < 8, g >= 8)
 };
 
 struct StreamMaps {
-    CUtensorMap codes; // uint32 {32, K/256, N}, box {32, kus, 16}, 128-byte swizzle
-    CUtensorMap steps; // uint16 {8, K/256, N},  box {8, kus, 16}
+    CUtensorMap codes; // uint32 {32, K/256, N}, box {32, kus, 64}, 128-byte swizzle
+    CUtensorMap steps; // uint16 {8, K/256, N},  box {8, kus, 64}
 };
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -110,19 +111,19 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
     const int C = (int)(gridDim.x / a.nclusters);
     const int crank = (C > 1) ? (int)cluster_rank() : 0;
     const int cid = blockIdx.x / C;
-    const int nrb = (a.N + 15) >> 4;
+    const int nrg = (a.N + kGroupRows - 1) / kGroupRows;
     const int nku = a.K >> 8;
-    const int rb0 = (int)((long long)cid * nrb / a.nclusters);
-    const int nrbc = (int)((long long)(cid + 1) * nrb / a.nclusters) - rb0;
+    const int g0 = (int)((long long)cid * nrg / a.nclusters);
+    const int ngc = (int)((long long)(cid + 1) * nrg / a.nclusters) - g0;
     const int ku0 = crank * (nku / C);  // C divides nku
-    const int sprb = (nku / C) / a.kus; // stages per row block; kus divides nku / C
-    const int nst = nrbc * sprb;
-    const int code_slot = a.kus * 2048, step_slot = a.kus * 256;
+    const int sprg = (nku / C) / a.kus; // stages per row group; kus divides nku / C
+    const int nst = ngc * sprg;
+    const int code_slot = a.kus * (kGroupRows * 128), step_slot = a.kus * (kGroupRows * 16);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.ns; ++i) {
             mbar_init(smem_addr(&full_bar[i]), 1);
-            mbar_init(smem_addr(&empty_bar[i]), 1);
+            mbar_init(smem_addr(&empty_bar[i]), kConsumerWarps);
         }
         s_abort = 0;
         fence_mbar_init();
@@ -134,8 +135,8 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 
     const uint32_t codes_ring = smem_addr(smem);
     const uint32_t steps_ring = codes_ring + a.off_steps;
-    float *spart = reinterpret_cast<float *>(smem + a.off_spart);
-    float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart);
+    float *spart = reinterpret_cast<float *>(smem + a.off_spart);   // [ngc][8 warps][MX][16]
+    float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart); // [ngc][4][MX][16]
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------- producer warp
@@ -144,20 +145,19 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
             const uint64_t pol = policy_evict_first();
             const uint32_t tx = (uint32_t)(code_slot + step_slot);
             for (int i = 0; i < nst; ++i) {
-                const int slot = (i % kConsumerWarps) + kConsumerWarps * ((i / kConsumerWarps) % a.dpw);
-                const int use = (i / kConsumerWarps) / a.dpw;
+                const int slot = i % a.ns, use = i / a.ns;
                 if (use > 0 && !mbar_wait_bounded(smem_addr(&empty_bar[slot]), (use - 1) & 1,
                                                   s_abort ? kDrainLimit : kWaitLimit)) {
                     s_abort = 1;
                     atomicOr(a.err, 1);
                 }
-                const int rbl = i / sprb, j = i - rbl * sprb;
-                const int rb = rb0 + rbl;
+                const int gl = i / sprg, j = i - gl * sprg;
                 const int kua = ku0 + j * a.kus;
+                const int row0 = (g0 + gl) * kGroupRows;
                 const uint32_t bar = smem_addr(&full_bar[slot]);
                 mbar_arrive_expect_tx(bar, tx);
-                tma_load_3d(codes_ring + slot * code_slot, &maps.codes, 0, kua, rb * 16, bar, pol);
-                tma_load_3d(steps_ring + slot * step_slot, &maps.steps, 0, kua, rb * 16, bar, pol);
+                tma_load_3d(codes_ring + slot * code_slot, &maps.codes, 0, kua, row0, bar, pol);
+                tma_load_3d(steps_ring + slot * step_slot, &maps.steps, 0, kua, row0, bar, pol);
             }
         }
     } else {
@@ -178,12 +178,17 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         const bool bsel = ((g & 3) == t) && (bm < MX);
         const uint4 *xrow = bsel ? xs + bm * cpr + 4 * t : xs + MX * cpr;
         const int xstep = bsel ? 16 : 0, xi = bsel ? 1 : 0;
-        const int ra = (int)((a.perm_lo >> (4 * g)) & 15u);  // weight row of mma row g
-        const int rbr = (int)((a.perm_hi >> (4 * g)) & 15u); // weight row of mma row g + 8
+        const int rbl = warp & 3;   // row block of the group this warp reads
+        const int khalf = warp >> 2; // which half of each stage's k-tiles
+        // weight rows (within the 64-row group) of mma rows g and g + 8
+        const int ra = rbl * 16 + (int)((a.perm_lo >> (4 * g)) & 15u);
+        const int rbr = rbl * 16 + (int)((a.perm_hi >> (4 * g)) & 15u);
+        const int la0 = ra * a.kus, lb0 = rbr * a.kus; // first 128-byte line of each row
+        const int spoff_a = la0 * 16 + 4 * (t & 1), spoff_b = lb0 * 16 + 4 * (t & 1);
 
-        for (int i = warp; i < nst; i += kConsumerWarps) {
-            const int slot = warp + kConsumerWarps * ((i / kConsumerWarps) % a.dpw);
-            const int use = (i / kConsumerWarps) / a.dpw;
+        float accA = 0.f, accB = 0.f;
+        for (int i = 0; i < nst; ++i) {
+            const int slot = i % a.ns, use = i / a.ns;
             if (!mbar_wait_bounded(smem_addr(&full_bar[slot]), use & 1,
                                    s_abort ? kDrainLimit : kWaitLimit)) {
                 if (lane == 0) {
@@ -191,25 +196,21 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                     atomicOr(a.err, 1);
                 }
             }
-            const int rbl = i / sprb, j = i - rbl * sprb;
+            const int gl = i / sprg, j = i - gl * sprg;
             const int kua = ku0 + j * a.kus;
             const unsigned char *cb = smem + slot * code_slot;
             const unsigned char *sb = smem + a.off_steps + slot * step_slot;
-            const int la0 = ra * a.kus, lb0 = rbr * a.kus; // first 128-byte line of each row
-            const unsigned char *pa = sb + la0 * 16 + 4 * (t & 1);
-            const unsigned char *pb = sb + lb0 * 16 + 4 * (t & 1);
             const uint4 *xb0 = xrow + xstep * (2 * kua);
-            float accA = 0.f, accB = 0.f;
-#pragma unroll 2
-            for (int kt = 0; kt < 2 * a.kus; ++kt) {
+            for (int kk = 0; kk < a.kus; ++kk) {
+                const int kt = khalf * a.kus + kk; // k-tile of the stage (0 .. 2*kus-1)
                 const int u = kt >> 1, ch = 4 * (kt & 1) + t;
                 const int la = la0 + u, lb = lb0 + u;
                 const uint4 wa =
                     *reinterpret_cast<const uint4 *>(cb + la * 128 + ((ch ^ (la & 7)) << 4));
                 const uint4 wb =
                     *reinterpret_cast<const uint4 *>(cb + lb * 128 + ((ch ^ (lb & 7)) << 4));
-                const uint32_t sa = *reinterpret_cast<const uint32_t *>(pa + u * 16 + 8 * (kt & 1));
-                const uint32_t sbv = *reinterpret_cast<const uint32_t *>(pb + u * 16 + 8 * (kt & 1));
+                const uint32_t sa = *reinterpret_cast<const uint32_t *>(sb + spoff_a + u * 16 + 8 * (kt & 1));
+                const uint32_t sbv = *reinterpret_cast<const uint32_t *>(sb + spoff_b + u * 16 + 8 * (kt & 1));
                 const uint4 *xb = xb0 + xstep * kt;
                 const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w};
                 const uint32_t bw[4] = {wb.x, wb.y, wb.z, wb.w};
@@ -231,24 +232,29 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_addr(&empty_bar[slot]));
-            accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
-            accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
-            const int m = t >> 1;
-            if ((t & 1) == 0 && m < MX) {
-                spart[(i * MX + m) * 16 + ra] = accA;
-                spart[(i * MX + m) * 16 + rbr] = accB;
+            if (j == sprg - 1) {
+                // End of this row group's K slice: park the warp's partials.
+                const float pA = accA + __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
+                const float pB = accB + __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+                const int m = t >> 1;
+                if ((t & 1) == 0 && m < MX) {
+                    float *sp = spart + ((gl * kConsumerWarps + warp) * MX + m) * 16;
+                    sp[ra - rbl * 16] = pA;
+                    sp[rbr - rbl * 16] = pB;
+                }
+                accA = accB = 0.f;
             }
         }
         named_sync(1, kConsumers);
 
-        // Each row block: sum of its stages in stage order.
-        for (int e = threadIdx.x; e < nrbc * MX * 16; e += kConsumers) {
-            const int rr = e & 15, m = (e >> 4) % MX, rbl = e / (16 * MX);
-            float s = 0.f;
-            for (int j = 0; j < sprb; ++j)
-                s += spart[((rbl * sprb + j) * MX + m) * 16 + rr];
+        // Row block rbl of group gl: its two k-halves (warps rbl, rbl + 4) in order.
+        for (int e = threadIdx.x; e < ngc * 4 * MX * 16; e += kConsumers) {
+            const int rr = e & 15, m = (e >> 4) % MX, q = e / (16 * MX);
+            const int gl = q >> 2, rb = q & 3;
+            const float s = spart[((gl * kConsumerWarps + rb) * MX + m) * 16 + rr] +
+                            spart[((gl * kConsumerWarps + rb + 4) * MX + m) * 16 + rr];
             if (C == 1)
-                emit(a, m, (rb0 + rbl) * 16 + rr, s, s_key, ARGMAX);
+                emit(a, m, (g0 + gl) * kGroupRows + rb * 16 + rr, s, s_key, ARGMAX);
             else
                 rbpart[e] = s;
         }
@@ -259,15 +265,15 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         // rank r writes elements [r*E/C, (r+1)*E/C) of the cluster's rows.
         cluster_sync();
         if (warp < kConsumerWarps) {
-            const int E = nrbc * MX * 16;
+            const int E = ngc * 4 * MX * 16;
             const int e0 = (int)((long long)crank * E / C), e1 = (int)((long long)(crank + 1) * E / C);
             const uint32_t base = smem_addr(rbpart);
             for (int e = e0 + threadIdx.x; e < e1; e += kConsumers) {
                 float s = 0.f;
                 for (int c = 0; c < C; ++c)
                     s += ld_cluster_f32(map_rank(base + 4u * e, (uint32_t)c));
-                const int rr = e & 15, m = (e >> 4) % MX, rbl = e / (16 * MX);
-                emit(a, m, (rb0 + rbl) * 16 + rr, s, s_key, ARGMAX);
+                const int rr = e & 15, m = (e >> 4) % MX, q = e / (16 * MX);
+                emit(a, m, (g0 + (q >> 2)) * kGroupRows + (q & 3) * 16 + rr, s, s_key, ARGMAX);
             }
         }
         cluster_sync(); // no CTA leaves while another still reads its shared memory
@@ -294,48 +300,52 @@ int divisor_at_most(int n, int cap)
 }
 
 struct Geometry {
-    int C = 1, nclusters = 1, kus = 1, ns = 1, dpw = 1;
+    int C = 1, nclusters = 1, kus = 1, ns = 1;
     int off_steps = 0, off_x = 0, off_spart = 0, off_rbpart = 0, smem = 0;
     bool ok = false;
 };
 
+// Stage size and slot count for a given split: among kus in {3, 2, 1} that
+// divide the CTA's K slice, the one with the most bytes in flight (ties: larger).
 Geometry make_geometry(int M, int N, int K, int C, int nclusters)
 {
     Geometry G;
-    const int nrb = ceil_div(N, 16), nku = K / 256;
+    const int nrg = ceil_div(N, kGroupRows), nku = K / 256;
     if (nku % C != 0)
         return G;
     const int nkuc = nku / C;
-    G.C = C;
-    G.nclusters = nclusters;
-    G.kus = divisor_at_most(nkuc, 6);
-    const int sprb = nkuc / G.kus;
-    const int rbc_max = ceil_div(nrb, nclusters);
-    const int max_stages = rbc_max * sprb;
-    const int code_slot = G.kus * 2048, step_slot = G.kus * 256;
+    const int rgc_max = ceil_div(nrg, nclusters);
     const int x_bytes = M * K * 2 + 16;
-    const int spart_bytes = max_stages * M * 16 * 4;
-    const int rbpart_bytes = (C > 1) ? rbc_max * M * 16 * 4 : 0;
-    for (int dpw = 2; dpw >= 1; --dpw) {
-        int ns = kConsumerWarps * dpw;
+    const int spart_bytes = rgc_max * kConsumerWarps * M * 16 * 4;
+    const int rbpart_bytes = (C > 1) ? rgc_max * 4 * M * 16 * 4 : 0;
+    long long best = -1;
+    for (int kus = 3; kus >= 1; --kus) {
+        if (nkuc % kus != 0)
+            continue;
+        const int code_slot = kus * kGroupRows * 128, step_slot = kus * kGroupRows * 16;
+        const int max_stages = rgc_max * (nkuc / kus);
+        const int fixed = x_bytes + spart_bytes + rbpart_bytes + 1024 + 64;
+        int ns = (kSmemBudget - fixed) / (code_slot + step_slot);
+        if (ns > kMaxSlots)
+            ns = kMaxSlots;
         if (ns > max_stages)
             ns = max_stages;
-        const int off_steps = ns * code_slot;
-        const int off_x = (off_steps + ns * step_slot + 15) & ~15;
-        const int off_spart = (off_x + x_bytes + 15) & ~15;
-        const int off_rbpart = (off_spart + spart_bytes + 15) & ~15;
-        const int total = off_rbpart + rbpart_bytes + 1024; // + alignment slack
-        if (total > kSmemBudget)
+        if (ns < 1 || (ns < 2 && max_stages > 1))
             continue;
+        const long long inflight = (long long)ns * (code_slot + step_slot);
+        if (inflight <= best)
+            continue;
+        best = inflight;
+        G.C = C;
+        G.nclusters = nclusters;
+        G.kus = kus;
         G.ns = ns;
-        G.dpw = dpw;
-        G.off_steps = off_steps;
-        G.off_x = off_x;
-        G.off_spart = off_spart;
-        G.off_rbpart = off_rbpart;
-        G.smem = total;
+        G.off_steps = ns * code_slot;
+        G.off_x = (G.off_steps + ns * step_slot + 15) & ~15;
+        G.off_spart = (G.off_x + x_bytes + 15) & ~15;
+        G.off_rbpart = (G.off_spart + spart_bytes + 15) & ~15;
+        G.smem = G.off_rbpart + rbpart_bytes + 1024; // + alignment slack
         G.ok = true;
-        return G;
     }
     return G;
 }
@@ -389,7 +399,7 @@ bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, i
     {
         cuuint64_t dims[3] = {32, nku, (cuuint64_t)N};
         cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
-        cuuint32_t box[3] = {32, (cuuint32_t)kus, 16};
+        cuuint32_t box[3] = {32, (cuuint32_t)kus, (cuuint32_t)kGroupRows};
         if (enc(&m.codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -398,7 +408,7 @@ bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, i
     {
         cuuint64_t dims[3] = {8, nku, (cuuint64_t)N};
         cuuint64_t strides[2] = {16, (cuuint64_t)K / 16};
-        cuuint32_t box[3] = {8, (cuuint32_t)kus, 16};
+        cuuint32_t box[3] = {8, (cuuint32_t)kus, (cuuint32_t)kGroupRows};
         if (enc(&m.steps, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t *>(sc), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -444,25 +454,25 @@ bool stream_supported(int M, int N, int K, const void *qw, const void *sc)
 StreamPlan plan_stream(int M, int N, int K, int num_sms)
 {
     // Per-shape tiling: the cluster size C (K slices, C | K/256) and the number
-    // of clusters that minimise the largest per-CTA share, one CTA per SM;
-    // smaller tensor copies cost more per byte, so the share is weighted by
-    // (1 + 1/kus).
+    // of clusters (64-row groups split across them) that minimise the largest
+    // per-CTA share, one CTA per SM; a share in small tensor copies costs more
+    // per byte, weighted by (1 + 1/(2 kus)).
     StreamPlan best;
-    const int nrb = ceil_div(N, 16), nku = K / 256;
+    const int nrg = ceil_div(N, kGroupRows), nku = K / 256;
     double best_cost = -1.0;
     const int cands[] = {1, 2, 3, 4, 6, 8};
     for (int C : cands) {
         if (nku % C != 0)
             continue;
         int ncl = num_sms / C;
-        if (ncl > nrb)
-            ncl = nrb;
+        if (ncl > nrg)
+            ncl = nrg;
         if (ncl < 1)
             continue;
         const Geometry G = make_geometry(M, N, K, C, ncl);
         if (!G.ok)
             continue;
-        const double cost = (double)ceil_div(nrb, ncl) * (nku / C) * (1.0 + 1.0 / G.kus);
+        const double cost = (double)ceil_div(nrg, ncl) * (nku / C) * (1.0 + 0.5 / G.kus);
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
             best.C = C;
@@ -493,7 +503,6 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
     a.nclusters = G.nclusters;
     a.kus = G.kus;
     a.ns = G.ns;
-    a.dpw = G.dpw;
     a.off_steps = G.off_steps;
     a.off_x = G.off_x;
     a.off_spart = G.off_spart;
