@@ -11,24 +11,27 @@
 // under programmatic dependent launch, and HBM needs ~100 KB in flight per SM.
 // So each kernel:
 //   1. starts streaming its weight share into a shared-memory ring at once with
-//      3-D tensor copies (one op per stage: 64 rows x kus x 256 k of codes, and
-//      one for their steps), issued by a producer warp before the kernel waits
+//      3-D tensor copies (one op per stage for codes, one for steps), issued by
+//      a producer warp before the kernel waits
 //      on the previous one (griddepcontrol.wait); the stream overlaps the
 //      previous kernel and the launch gap;
 //   2. keeps every SM busy after the wait: rows are split across clusters in
-//      whole 64-row groups and K is split across the CTAs of a cluster, whose
+//      whole 16-row blocks and K is split across the CTAs of a cluster, whose
 //      partial sums are added through distributed shared memory in a fixed
 //      rank order (deterministic; no global scratch; no atomics on y);
 //   3. stays under half of an SM's shared memory so the next kernel's CTAs can
 //      be resident at the same time and stream their weights.
 //
-// Stages. A stage is 64 rows (4 row blocks) x kus ku of one CTA's K slice; all
-// 8 consumer warps read every stage (warp w: row block w & 3, k-tile half
-// w >> 2), so stages are consumed and their slots refilled in order and the
-// whole ring stays in flight. Codes arrive as [row][ku][128 B] with the
-// hardware's 128-byte swizzle (16-byte chunk c of line L lands at chunk
+// Stages. A stage is one 16-row block over the CTA's whole K slice, fetched
+// as one 3-D tensor copy of codes ({32 words, ku, 16 rows}: every row a
+// contiguous run of K-slice/2 bytes, which is what the copy engine streams
+// fastest) and one of steps. All 8 consumer warps read every stage, taking its
+// k-tiles in a rotation that balances over consecutive stages, so slots are
+// consumed and refilled in order and the whole ring stays in flight; the last
+// warp to finish a stage adds the 8 warps' partials in warp order. Codes land
+// with the hardware's 128-byte swizzle (16-byte chunk c of line L at chunk
 // c ^ (L & 7)); the mma row -> weight row map pairs rows whose lines differ in
-// bit 2 of L & 7, so every 8-lane phase of a 128-bit read touches all 32 banks
+// bit 2 of L & 7, so each 8-lane phase of a 128-bit read touches all 32 banks
 // once. Steps arrive as [row][ku][8 x bf16] without swizzle.
 //
 // Inner product: exact (code - 8) bf16 x bf16 m16n8k16 mma with fp32 accumulate.
@@ -51,7 +54,7 @@ constexpr int kMaxSlots = 16;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
-constexpr int kGroupRows = 64;       // rows per stage (4 row blocks of 16)
+constexpr int kMaxKu = 16;           // ku per stage (box depth; 4 KB of codes per row)
 constexpr int kWaitLimit = 1 << 22;  // polls before a wait is declared failed
 constexpr int kDrainLimit = 1 << 10; // polls per wait once a failure was seen
 constexpr int kSmemBudget = 110 * 1024;
@@ -62,17 +65,16 @@ struct StreamArgs {
     unsigned long long *keys; // argmax keys [MX][gridDim.x] or null
     int *err;                 // device error word (bit 0: a wait timed out)
     int N, K;
-    int nclusters;   // row-group ranges (one cluster each)
-    int kus;         // ku (256-k units) per stage
+    int nclusters;   // row-block ranges (one cluster each)
     int ns;          // ring slots
     int off_steps;   // offset of the steps ring (codes ring at the aligned base)
-    int off_x, off_spart, off_rbpart;
-    uint32_t perm_lo, perm_hi; // mma row g -> row of the block, 4 bits each (g < 8, g >= 8)
+    int off_x, off_red, off_rbpart;
+    uint32_t perm_lo, perm_hi; // mma row g -> weight row of the block, 4 bits each
 };
 
 struct StreamMaps {
-    CUtensorMap codes; // uint32 {32, K/256, N}, box {32, kus, 64}, 128-byte swizzle
-    CUtensorMap steps; // uint16 {8, K/256, N},  box {8, kus, 64}
+    CUtensorMap codes; // uint32 {32, K/256, N}, box {32, K/256/C, 16}, 128-byte swizzle
+    CUtensorMap steps; // uint16 {8, K/256, N},  box {8, K/256/C, 16}
 };
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -101,6 +103,7 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) unsigned long long full_bar[kMaxSlots];
     __shared__ __align__(8) unsigned long long empty_bar[kMaxSlots];
+    __shared__ int s_count[kMaxSlots];
     __shared__ int s_abort;
     __shared__ unsigned long long s_key[MX];
 
@@ -111,19 +114,19 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
     const int C = (int)(gridDim.x / a.nclusters);
     const int crank = (C > 1) ? (int)cluster_rank() : 0;
     const int cid = blockIdx.x / C;
-    const int nrg = (a.N + kGroupRows - 1) / kGroupRows;
-    const int nku = a.K >> 8;
-    const int g0 = (int)((long long)cid * nrg / a.nclusters);
-    const int ngc = (int)((long long)(cid + 1) * nrg / a.nclusters) - g0;
-    const int ku0 = crank * (nku / C);  // C divides nku
-    const int sprg = (nku / C) / a.kus; // stages per row group; kus divides nku / C
-    const int nst = ngc * sprg;
-    const int code_slot = a.kus * (kGroupRows * 128), step_slot = a.kus * (kGroupRows * 16);
+    const int nrb = (a.N + 15) >> 4;
+    const int nkuc = (a.K >> 8) / C; // ku of this CTA's K slice (C divides K/256)
+    const int ku0 = crank * nkuc;
+    const int ktiles = 2 * nkuc;     // 128-k tiles per stage
+    const int rb0 = (int)((long long)cid * nrb / a.nclusters);
+    const int nst = (int)((long long)(cid + 1) * nrb / a.nclusters) - rb0; // one stage per row block
+    const int code_slot = nkuc * 2048, step_slot = nkuc * 256;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.ns; ++i) {
             mbar_init(smem_addr(&full_bar[i]), 1);
             mbar_init(smem_addr(&empty_bar[i]), kConsumerWarps);
+            s_count[i] = 0;
         }
         s_abort = 0;
         fence_mbar_init();
@@ -135,8 +138,8 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 
     const uint32_t codes_ring = smem_addr(smem);
     const uint32_t steps_ring = codes_ring + a.off_steps;
-    float *spart = reinterpret_cast<float *>(smem + a.off_spart);   // [ngc][8 warps][MX][16]
-    float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart); // [ngc][4][MX][16]
+    float *red = reinterpret_cast<float *>(smem + a.off_red);       // [ns][8 warps][MX][16]
+    float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart); // [nst][MX][16] (C > 1)
 
     if (warp == kConsumerWarps) {
         // ---------------------------------------------------- producer warp
@@ -151,13 +154,10 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                     s_abort = 1;
                     atomicOr(a.err, 1);
                 }
-                const int gl = i / sprg, j = i - gl * sprg;
-                const int kua = ku0 + j * a.kus;
-                const int row0 = (g0 + gl) * kGroupRows;
                 const uint32_t bar = smem_addr(&full_bar[slot]);
                 mbar_arrive_expect_tx(bar, tx);
-                tma_load_3d(codes_ring + slot * code_slot, &maps.codes, 0, kua, row0, bar, pol);
-                tma_load_3d(steps_ring + slot * step_slot, &maps.steps, 0, kua, row0, bar, pol);
+                tma_load_3d(codes_ring + slot * code_slot, &maps.codes, 0, ku0, (rb0 + i) * 16, bar, pol);
+                tma_load_3d(steps_ring + slot * step_slot, &maps.steps, 0, ku0, (rb0 + i) * 16, bar, pol);
             }
         }
     } else {
@@ -176,17 +176,14 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         const int g = lane >> 2, t = lane & 3;
         const int bm = g >> 2;
         const bool bsel = ((g & 3) == t) && (bm < MX);
-        const uint4 *xrow = bsel ? xs + bm * cpr + 4 * t : xs + MX * cpr;
+        const uint4 *xrow = (bsel ? xs + bm * cpr + 4 * t : xs + MX * cpr);
         const int xstep = bsel ? 16 : 0, xi = bsel ? 1 : 0;
-        const int rbl = warp & 3;   // row block of the group this warp reads
-        const int khalf = warp >> 2; // which half of each stage's k-tiles
-        // weight rows (within the 64-row group) of mma rows g and g + 8
-        const int ra = rbl * 16 + (int)((a.perm_lo >> (4 * g)) & 15u);
-        const int rbr = rbl * 16 + (int)((a.perm_hi >> (4 * g)) & 15u);
-        const int la0 = ra * a.kus, lb0 = rbr * a.kus; // first 128-byte line of each row
+        const uint4 *xb0 = xrow + xstep * (2 * ku0);
+        const int ra = (int)((a.perm_lo >> (4 * g)) & 15u);  // weight row of mma row g
+        const int rbr = (int)((a.perm_hi >> (4 * g)) & 15u); // weight row of mma row g + 8
+        const int la0 = ra * nkuc, lb0 = rbr * nkuc;         // first 128-byte line of each row
         const int spoff_a = la0 * 16 + 4 * (t & 1), spoff_b = lb0 * 16 + 4 * (t & 1);
 
-        float accA = 0.f, accB = 0.f;
         for (int i = 0; i < nst; ++i) {
             const int slot = i % a.ns, use = i / a.ns;
             if (!mbar_wait_bounded(smem_addr(&full_bar[slot]), use & 1,
@@ -196,13 +193,12 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                     atomicOr(a.err, 1);
                 }
             }
-            const int gl = i / sprg, j = i - gl * sprg;
-            const int kua = ku0 + j * a.kus;
             const unsigned char *cb = smem + slot * code_slot;
             const unsigned char *sb = smem + a.off_steps + slot * step_slot;
-            const uint4 *xb0 = xrow + xstep * (2 * kua);
-            for (int kk = 0; kk < a.kus; ++kk) {
-                const int kt = khalf * a.kus + kk; // k-tile of the stage (0 .. 2*kus-1)
+            float accA = 0.f, accB = 0.f;
+            // k-tiles kt = first, first + 8, ... ; the rotation balances the warps
+            const int first = (int)(((unsigned)warp + 8u * 1024u - (unsigned)((i * ktiles) & 7)) & 7u);
+            for (int kt = first; kt < ktiles; kt += kConsumerWarps) {
                 const int u = kt >> 1, ch = 4 * (kt & 1) + t;
                 const int la = la0 + u, lb = lb0 + u;
                 const uint4 wa =
@@ -229,34 +225,43 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                 accB = fmaf(bf16lo_to_f32(sbv), c[2], accB);
                 accB = fmaf(bf16hi_to_f32(sbv), c[3], accB);
             }
+            // This warp's partial of the row block -> red[slot][warp].
+            accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
+            accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+            const int m = t >> 1;
+            float *rs = red + slot * (kConsumerWarps * MX * 16);
+            if ((t & 1) == 0 && m < MX) {
+                rs[(warp * MX + m) * 16 + ra] = accA;
+                rs[(warp * MX + m) * 16 + rbr] = accB;
+            }
             __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = (atomicAdd(&s_count[slot], 1) == kConsumerWarps - 1);
+                if (last)
+                    __threadfence_block();
+            }
+            last = __shfl_sync(0xFFFFFFFFu, last, 0);
+            if (last) {
+                // Sum the 8 warps' partials in warp order; reset the counter
+                // before the slot is released.
+                if (lane < MX * 16) {
+                    float s = 0.f;
+                    for (int w = 0; w < kConsumerWarps; ++w)
+                        s += rs[w * MX * 16 + lane];
+                    const int mm = lane >> 4, rr = lane & 15;
+                    if (C == 1)
+                        emit(a, mm, (rb0 + i) * 16 + rr, s, s_key, ARGMAX);
+                    else
+                        rbpart[i * MX * 16 + lane] = s;
+                }
+                if (lane == 0)
+                    s_count[slot] = 0;
+                __syncwarp();
+            }
             if (lane == 0)
                 mbar_arrive(smem_addr(&empty_bar[slot]));
-            if (j == sprg - 1) {
-                // End of this row group's K slice: park the warp's partials.
-                const float pA = accA + __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
-                const float pB = accB + __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
-                const int m = t >> 1;
-                if ((t & 1) == 0 && m < MX) {
-                    float *sp = spart + ((gl * kConsumerWarps + warp) * MX + m) * 16;
-                    sp[ra - rbl * 16] = pA;
-                    sp[rbr - rbl * 16] = pB;
-                }
-                accA = accB = 0.f;
-            }
-        }
-        named_sync(1, kConsumers);
-
-        // Row block rbl of group gl: its two k-halves (warps rbl, rbl + 4) in order.
-        for (int e = threadIdx.x; e < ngc * 4 * MX * 16; e += kConsumers) {
-            const int rr = e & 15, m = (e >> 4) % MX, q = e / (16 * MX);
-            const int gl = q >> 2, rb = q & 3;
-            const float s = spart[((gl * kConsumerWarps + rb) * MX + m) * 16 + rr] +
-                            spart[((gl * kConsumerWarps + rb + 4) * MX + m) * 16 + rr];
-            if (C == 1)
-                emit(a, m, (g0 + gl) * kGroupRows + rb * 16 + rr, s, s_key, ARGMAX);
-            else
-                rbpart[e] = s;
         }
     }
 
@@ -265,7 +270,7 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         // rank r writes elements [r*E/C, (r+1)*E/C) of the cluster's rows.
         cluster_sync();
         if (warp < kConsumerWarps) {
-            const int E = ngc * 4 * MX * 16;
+            const int E = nst * MX * 16;
             const int e0 = (int)((long long)crank * E / C), e1 = (int)((long long)(crank + 1) * E / C);
             const uint32_t base = smem_addr(rbpart);
             for (int e = e0 + threadIdx.x; e < e1; e += kConsumers) {
@@ -273,7 +278,7 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                 for (int c = 0; c < C; ++c)
                     s += ld_cluster_f32(map_rank(base + 4u * e, (uint32_t)c));
                 const int rr = e & 15, m = (e >> 4) % MX, q = e / (16 * MX);
-                emit(a, m, (g0 + (q >> 2)) * kGroupRows + (q & 3) * 16 + rr, s, s_key, ARGMAX);
+                emit(a, m, (rb0 + q) * 16 + rr, s, s_key, ARGMAX);
             }
         }
         cluster_sync(); // no CTA leaves while another still reads its shared memory
@@ -290,70 +295,50 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Largest divisor of n that is <= cap.
-int divisor_at_most(int n, int cap)
-{
-    for (int d = cap; d >= 1; --d)
-        if (n % d == 0)
-            return d;
-    return 1;
-}
-
 struct Geometry {
-    int C = 1, nclusters = 1, kus = 1, ns = 1;
-    int off_steps = 0, off_x = 0, off_spart = 0, off_rbpart = 0, smem = 0;
+    int C = 1, nclusters = 1, ns = 1;
+    int off_steps = 0, off_x = 0, off_red = 0, off_rbpart = 0, smem = 0;
     bool ok = false;
 };
 
-// Stage size and slot count for a given split: among kus in {3, 2, 1} that
-// divide the CTA's K slice, the one with the most bytes in flight (ties: larger).
+// Ring for a given split: as many whole-stage slots as the budget allows.
 Geometry make_geometry(int M, int N, int K, int C, int nclusters)
 {
     Geometry G;
-    const int nrg = ceil_div(N, kGroupRows), nku = K / 256;
-    if (nku % C != 0)
+    const int nrb = ceil_div(N, 16), nku = K / 256;
+    if (nku % C != 0 || nku / C > kMaxKu)
         return G;
     const int nkuc = nku / C;
-    const int rgc_max = ceil_div(nrg, nclusters);
+    const int max_stages = ceil_div(nrb, nclusters);
+    const int code_slot = nkuc * 2048, step_slot = nkuc * 256;
+    const int red_slot = kConsumerWarps * M * 16 * 4;
     const int x_bytes = M * K * 2 + 16;
-    const int spart_bytes = rgc_max * kConsumerWarps * M * 16 * 4;
-    const int rbpart_bytes = (C > 1) ? rgc_max * 4 * M * 16 * 4 : 0;
-    long long best = -1;
-    for (int kus = 3; kus >= 1; --kus) {
-        if (nkuc % kus != 0)
-            continue;
-        const int code_slot = kus * kGroupRows * 128, step_slot = kus * kGroupRows * 16;
-        const int max_stages = rgc_max * (nkuc / kus);
-        const int fixed = x_bytes + spart_bytes + rbpart_bytes + 1024 + 64;
-        int ns = (kSmemBudget - fixed) / (code_slot + step_slot);
-        if (ns > kMaxSlots)
-            ns = kMaxSlots;
-        if (ns > max_stages)
-            ns = max_stages;
-        if (ns < 1 || (ns < 2 && max_stages > 1))
-            continue;
-        const long long inflight = (long long)ns * (code_slot + step_slot);
-        if (inflight <= best)
-            continue;
-        best = inflight;
-        G.C = C;
-        G.nclusters = nclusters;
-        G.kus = kus;
-        G.ns = ns;
-        G.off_steps = ns * code_slot;
-        G.off_x = (G.off_steps + ns * step_slot + 15) & ~15;
-        G.off_spart = (G.off_x + x_bytes + 15) & ~15;
-        G.off_rbpart = (G.off_spart + spart_bytes + 15) & ~15;
-        G.smem = G.off_rbpart + rbpart_bytes + 1024; // + alignment slack
-        G.ok = true;
-    }
+    const int rbpart_bytes = (C > 1) ? max_stages * M * 16 * 4 : 0;
+    const int fixed = x_bytes + rbpart_bytes + 1024 + 64;
+    int ns = (kSmemBudget - fixed) / (code_slot + step_slot + red_slot);
+    if (ns > kMaxSlots)
+        ns = kMaxSlots;
+    if (ns > max_stages)
+        ns = max_stages;
+    if (ns < 1 || (ns < 2 && max_stages > 1))
+        return G;
+    G.C = C;
+    G.nclusters = nclusters;
+    G.ns = ns;
+    G.off_steps = ns * code_slot;
+    G.off_x = (G.off_steps + ns * step_slot + 15) & ~15;
+    G.off_red = (G.off_x + x_bytes + 15) & ~15;
+    G.off_rbpart = (G.off_red + ns * red_slot + 15) & ~15;
+    G.smem = G.off_rbpart + rbpart_bytes + 1024; // + alignment slack
+    G.ok = true;
     return G;
 }
 
 // mma row -> weight row map that keeps 128-bit reads of the swizzled codes
 // conflict-free: the two rows read by one 8-lane phase differ in bit 2 of
 // (row * kus + u) & 7 for every u < kus (pairs r, r+4 for odd kus; r, r+2 for
-// kus = 2 mod 4; r, r+1 for kus = 0 mod 4).
+// kus = 2 mod 4; r, r+1 for kus = 4 mod 8; kus = 0 mod 8 has no such pairing
+// and reads with two-way conflicts).
 void row_perm(int kus, uint32_t &lo, uint32_t &hi)
 {
     int p[16];
@@ -399,7 +384,7 @@ bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, i
     {
         cuuint64_t dims[3] = {32, nku, (cuuint64_t)N};
         cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
-        cuuint32_t box[3] = {32, (cuuint32_t)kus, (cuuint32_t)kGroupRows};
+        cuuint32_t box[3] = {32, (cuuint32_t)kus, 16};
         if (enc(&m.codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -408,7 +393,7 @@ bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, i
     {
         cuuint64_t dims[3] = {8, nku, (cuuint64_t)N};
         cuuint64_t strides[2] = {16, (cuuint64_t)K / 16};
-        cuuint32_t box[3] = {8, (cuuint32_t)kus, (cuuint32_t)kGroupRows};
+        cuuint32_t box[3] = {8, (cuuint32_t)kus, 16};
         if (enc(&m.steps, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t *>(sc), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -453,27 +438,30 @@ bool stream_supported(int M, int N, int K, const void *qw, const void *sc)
 
 StreamPlan plan_stream(int M, int N, int K, int num_sms)
 {
-    // Per-shape tiling: the cluster size C (K slices, C | K/256) and the number
-    // of clusters (64-row groups split across them) that minimise the largest
-    // per-CTA share, one CTA per SM; a share in small tensor copies costs more
-    // per byte, weighted by (1 + 1/(2 kus)).
+    // Per-shape tiling: cluster size C (K slices, C | K/256, at most 16 ku per
+    // slice) and the number of clusters (16-row blocks split across them), one
+    // CTA per SM. Modelled time of the busiest CTA: its stages, each costing the
+    // larger of the copy engine's per-row cost (~40 cycles per row segment) and
+    // the segment's bytes at ~24 B/cycle.
     StreamPlan best;
-    const int nrg = ceil_div(N, kGroupRows), nku = K / 256;
+    const int nrb = ceil_div(N, 16), nku = K / 256;
     double best_cost = -1.0;
     const int cands[] = {1, 2, 3, 4, 6, 8};
     for (int C : cands) {
-        if (nku % C != 0)
+        if (nku % C != 0 || nku / C > kMaxKu)
             continue;
         int ncl = num_sms / C;
-        if (ncl > nrg)
-            ncl = nrg;
+        if (ncl > nrb)
+            ncl = nrb;
         if (ncl < 1)
             continue;
         const Geometry G = make_geometry(M, N, K, C, ncl);
         if (!G.ok)
             continue;
-        const double cost = (double)ceil_div(nrg, ncl) * (nku / C) * (1.0 + 0.5 / G.kus);
-        if (best_cost < 0 || cost < best_cost) {
+        const double seg = (double)(nku / C) * 128.0;
+        const double per_stage = 16.0 * (seg / 24.0 > 40.0 ? seg / 24.0 : 40.0);
+        const double cost = (double)ceil_div(nrb, ncl) * per_stage;
+        if (best_cost < 0 || cost < best_cost * 0.999) {
             best_cost = cost;
             best.C = C;
             best.nclusters = ncl;
@@ -490,8 +478,9 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
     const Geometry G = make_geometry(M, N, K, p.C, p.nclusters);
     if (!G.ok)
         return cudaErrorInvalidConfiguration;
+    const int nkuc = (K / 256) / G.C;
     StreamMaps maps;
-    if (!encode_maps(maps, qw, sc, N, K, G.kus))
+    if (!encode_maps(maps, qw, sc, N, K, nkuc))
         return cudaErrorInvalidValue;
     StreamArgs a;
     a.y = y;
@@ -501,13 +490,12 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
     a.N = N;
     a.K = K;
     a.nclusters = G.nclusters;
-    a.kus = G.kus;
     a.ns = G.ns;
     a.off_steps = G.off_steps;
     a.off_x = G.off_x;
-    a.off_spart = G.off_spart;
+    a.off_red = G.off_red;
     a.off_rbpart = G.off_rbpart;
-    row_perm(G.kus, a.perm_lo, a.perm_hi);
+    row_perm(nkuc, a.perm_lo, a.perm_hi);
     const bool am = argmax != nullptr;
     cudaError_t e;
     if (M == 1)
