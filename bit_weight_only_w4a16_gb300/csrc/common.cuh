@@ -64,8 +64,9 @@ __device__ __forceinline__ void pdl_wait()
 // of the "OR into the bits of 2^23 and subtract 2^23 + 8" unpack.
 __device__ __forceinline__ uint32_t nib_pair_bf16(uint32_t w)
 {
-    uint32_t t = (w & 0x000F000Fu) | 0x43004300u;
-    uint32_t r;
+    uint32_t t, r;
+    // (w & 0x000F000F) | 0x43004300 in one three-input logic op
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(t) : "r"(w), "r"(0x000F000Fu), "r"(0x43004300u));
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x43084308u));
     return r;
 }

@@ -117,7 +117,6 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
     const int nrb = (a.N + 15) >> 4;
     const int nkuc = (a.K >> 8) / C; // ku of this CTA's K slice (C divides K/256)
     const int ku0 = crank * nkuc;
-    const int ktiles = 2 * nkuc;     // 128-k tiles per stage
     const int rb0 = (int)((long long)cid * nrb / a.nclusters);
     const int nst = (int)((long long)(cid + 1) * nrb / a.nclusters) - rb0; // one stage per row block
     const int code_slot = nkuc * 2048, step_slot = nkuc * 256;
@@ -182,7 +181,6 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         const int ra = (int)((a.perm_lo >> (4 * g)) & 15u);  // weight row of mma row g
         const int rbr = (int)((a.perm_hi >> (4 * g)) & 15u); // weight row of mma row g + 8
         const int la0 = ra * nkuc, lb0 = rbr * nkuc;         // first 128-byte line of each row
-        const int spoff_a = la0 * 16 + 4 * (t & 1), spoff_b = lb0 * 16 + 4 * (t & 1);
 
         for (int i = 0; i < nst; ++i) {
             const int slot = i % a.ns, use = i / a.ns;
@@ -193,37 +191,48 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                     atomicOr(a.err, 1);
                 }
             }
-            const unsigned char *cb = smem + slot * code_slot;
-            const unsigned char *sb = smem + a.off_steps + slot * step_slot;
+            const uint32_t cb = codes_ring + slot * code_slot;
+            const uint32_t sbase = steps_ring + slot * step_slot;
             float accA = 0.f, accB = 0.f;
-            // k-tiles kt = first, first + 8, ... ; the rotation balances the warps
-            const int first = (int)(((unsigned)warp + 8u * 1024u - (unsigned)((i * ktiles) & 7)) & 7u);
-            for (int kt = first; kt < ktiles; kt += kConsumerWarps) {
-                const int u = kt >> 1, ch = 4 * (kt & 1) + t;
+            // 256-k units u = first, first + 8, ...; the rotation balances the
+            // warps over consecutive stages.
+            const int first = (int)(((unsigned)warp + 8u * 4096u - (unsigned)((i * nkuc) & 7)) & 7u);
+            for (int u = first; u < nkuc; u += kConsumerWarps) {
                 const int la = la0 + u, lb = lb0 + u;
-                const uint4 wa =
-                    *reinterpret_cast<const uint4 *>(cb + la * 128 + ((ch ^ (la & 7)) << 4));
-                const uint4 wb =
-                    *reinterpret_cast<const uint4 *>(cb + lb * 128 + ((ch ^ (lb & 7)) << 4));
-                const uint32_t sa = *reinterpret_cast<const uint32_t *>(sb + spoff_a + u * 16 + 8 * (kt & 1));
-                const uint32_t sbv = *reinterpret_cast<const uint32_t *>(sb + spoff_b + u * 16 + 8 * (kt & 1));
-                const uint4 *xb = xb0 + xstep * kt;
-                const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w};
-                const uint32_t bw[4] = {wb.x, wb.y, wb.z, wb.w};
-                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                // 16-byte chunk t of k-tile 0 and chunk 4 + t of k-tile 1, swizzled
+                const uint32_t qa0 = cb + la * 128 + ((t ^ (la & 7)) << 4);
+                const uint32_t qb0 = cb + lb * 128 + ((t ^ (lb & 7)) << 4);
+                const uint4 wa0 = lds128(qa0), wa1 = lds128(qa0 ^ 64u);
+                const uint4 wb0 = lds128(qb0), wb1 = lds128(qb0 ^ 64u);
+                const uint32_t pa = sbase + la * 16 + 4 * (t & 1);
+                const uint32_t pb = sbase + lb * 16 + 4 * (t & 1);
+                const uint32_t sa0 = lds32(pa), sa1 = lds32(pa + 8);
+                const uint32_t sb0 = lds32(pb), sb1 = lds32(pb + 8);
+                const uint4 *xb = xb0 + xstep * (2 * u);
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t a0w[4] = {wa0.x, wa0.y, wa0.z, wa0.w}, b0w[4] = {wb0.x, wb0.y, wb0.z, wb0.w};
+                const uint32_t a1w[4] = {wa1.x, wa1.y, wa1.z, wa1.w}, b1w[4] = {wb1.x, wb1.y, wb1.z, wb1.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint4 b = xb[xi * q];
+                    const uint4 x0 = xb[xi * q], x1 = xb[xstep + xi * q];
                     uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
-                    unpack_word(aw[q], a04, a15, a26, a37);
-                    unpack_word(bw[q], b04, b15, b26, b37);
-                    mma_16816(c, a04, b04, a15, b15, b.x, b.y);
-                    mma_16816(c, a26, b26, a37, b37, b.z, b.w);
+                    unpack_word(a0w[q], a04, a15, a26, a37);
+                    unpack_word(b0w[q], b04, b15, b26, b37);
+                    mma_16816(c0, a04, b04, a15, b15, x0.x, x0.y);
+                    mma_16816(c0, a26, b26, a37, b37, x0.z, x0.w);
+                    unpack_word(a1w[q], a04, a15, a26, a37);
+                    unpack_word(b1w[q], b04, b15, b26, b37);
+                    mma_16816(c1, a04, b04, a15, b15, x1.x, x1.y);
+                    mma_16816(c1, a26, b26, a37, b37, x1.z, x1.w);
                 }
-                accA = fmaf(bf16lo_to_f32(sa), c[0], accA);
-                accA = fmaf(bf16hi_to_f32(sa), c[1], accA);
-                accB = fmaf(bf16lo_to_f32(sbv), c[2], accB);
-                accB = fmaf(bf16hi_to_f32(sbv), c[3], accB);
+                accA = fmaf(bf16lo_to_f32(sa0), c0[0], accA);
+                accA = fmaf(bf16hi_to_f32(sa0), c0[1], accA);
+                accB = fmaf(bf16lo_to_f32(sb0), c0[2], accB);
+                accB = fmaf(bf16hi_to_f32(sb0), c0[3], accB);
+                accA = fmaf(bf16lo_to_f32(sa1), c1[0], accA);
+                accA = fmaf(bf16hi_to_f32(sa1), c1[1], accA);
+                accB = fmaf(bf16lo_to_f32(sb1), c1[2], accB);
+                accB = fmaf(bf16hi_to_f32(sb1), c1[3], accB);
             }
             // This warp's partial of the row block -> red[slot][warp].
             accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
