@@ -25,10 +25,10 @@
 // Stages. A stage is one 16-row block over the CTA's whole K slice, fetched
 // as one 3-D tensor copy of codes ({32 words, ku, 16 rows}: every row a
 // contiguous run of K-slice/2 bytes, which is what the copy engine streams
-// fastest) and one of steps. All 8 consumer warps read every stage, taking its
-// k-tiles in a rotation that balances over consecutive stages, so slots are
+// fastest) and one of steps. All 12 consumer warps read every stage, taking its
+// 256-k units in a rotation that balances over consecutive stages, so slots are
 // consumed and refilled in order and the whole ring stays in flight; the last
-// warp to finish a stage adds the 8 warps' partials in warp order. Codes land
+// warp to finish a stage adds the warps' partials in warp order. Codes land
 // with the hardware's 128-byte swizzle (16-byte chunk c of line L at chunk
 // c ^ (L & 7)); the mma row -> weight row map pairs rows whose lines differ in
 // bit 2 of L & 7, so each 8-lane phase of a 128-bit read touches all 32 banks
@@ -51,7 +51,7 @@ namespace w4 {
 namespace {
 
 constexpr int kMaxSlots = 16;
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 12;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kMaxKu = 16;           // ku per stage (box depth; 4 KB of codes per row)
@@ -196,7 +196,7 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
             float accA = 0.f, accB = 0.f;
             // 256-k units u = first, first + 8, ...; the rotation balances the
             // warps over consecutive stages.
-            const int first = (int)(((unsigned)warp + 8u * 4096u - (unsigned)((i * nkuc) & 7)) & 7u);
+            const int first = (int)((((unsigned)warp + (unsigned)kConsumerWarps * 4096u) - (unsigned)((i * nkuc) % kConsumerWarps)) % (unsigned)kConsumerWarps);
             for (int u = first; u < nkuc; u += kConsumerWarps) {
                 const int la = la0 + u, lb = lb0 + u;
                 // 16-byte chunk t of k-tile 0 and chunk 4 + t of k-tile 1, swizzled
@@ -253,7 +253,7 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
             }
             last = __shfl_sync(0xFFFFFFFFu, last, 0);
             if (last) {
-                // Sum the 8 warps' partials in warp order; reset the counter
+                // Sum the warps' partials in warp order; reset the counter
                 // before the slot is released.
                 if (lane < MX * 16) {
                     float s = 0.f;
