@@ -121,23 +121,26 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+// One potentially blocking test of an mbarrier phase: the thread sleeps until
+// the phase completes or about `hint_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns)
 {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.shared.b64 p, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared.b64 p, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok)
-                 : "r"(bar), "r"(parity)
+                 : "r"(bar), "r"(parity), "r"(hint_ns)
                  : "memory");
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase: false after `limit` polls (never hangs).
+// Bounded wait on an mbarrier phase: false after `limit` tests of up to
+// ~20 us each (never hangs).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int limit)
 {
     for (int i = 0; i < limit; ++i)
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait(bar, parity, 20000u))
             return true;
     return false;
 }

@@ -22,17 +22,19 @@
 //   3. stays under half of an SM's shared memory so the next kernel's CTAs can
 //      be resident at the same time and stream their weights.
 //
-// Stages. A stage is one 16-row block over the CTA's whole K slice, fetched
-// as one 3-D tensor copy of codes ({32 words, ku, 16 rows}: every row a
-// contiguous run of K-slice/2 bytes, which is what the copy engine streams
-// fastest) and one of steps. All 12 consumer warps read every stage, taking its
-// 256-k units in a rotation that balances over consecutive stages, so slots are
-// consumed and refilled in order and the whole ring stays in flight; the last
-// warp to finish a stage adds the warps' partials in warp order. Codes land
-// with the hardware's 128-byte swizzle (16-byte chunk c of line L at chunk
-// c ^ (L & 7)); the mma row -> weight row map pairs rows whose lines differ in
-// bit 2 of L & 7, so each 8-lane phase of a 128-bit read touches all 32 banks
-// once. Steps arrive as [row][ku][8 x bf16] without swizzle.
+// Stages. A stage is SR 16-row blocks (SR = 1 or 2) over the CTA's whole K
+// slice, fetched as one 3-D tensor copy of codes ({32 words, ku, 16 SR rows}:
+// every row a contiguous run of K-slice/2 bytes, which is what the copy engine
+// streams fastest) and one of steps. Consumer warp w owns the fixed k-tiles
+// w*KPW .. w*KPW + KPW - 1 of the slice (W * KPW = k-tiles per slice), so its
+// B fragments (x) are loaded into registers once per kernel and each stage
+// costs it only two 128-bit and two 32-bit shared loads per k-tile. Every warp
+// reads every stage, so slots are consumed and refilled in order and the whole
+// ring stays in flight; the last warp to finish a stage adds the W partials in
+// warp order. Codes land with the hardware's 128-byte swizzle (16-byte chunk c
+// of line L at chunk c ^ (L & 7)); the mma row -> weight row map pairs rows
+// whose lines differ in bit 2 of L & 7, so each 8-lane phase of a 128-bit read
+// touches all 32 banks once. Steps arrive as [row][ku][8 x bf16], unswizzled.
 //
 // Inner product: exact (code - 8) bf16 x bf16 m16n8k16 mma with fp32 accumulate.
 // Lane (g, t) holds group 4*kt + t of two weight rows; B column 4*m + s carries
@@ -51,12 +53,10 @@ namespace w4 {
 namespace {
 
 constexpr int kMaxSlots = 16;
-constexpr int kConsumerWarps = 12;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
-constexpr int kMaxKu = 16;           // ku per stage (box depth; 4 KB of codes per row)
-constexpr int kWaitLimit = 1 << 22;  // polls before a wait is declared failed
-constexpr int kDrainLimit = 1 << 10; // polls per wait once a failure was seen
+constexpr int kMaxWarps = 12;        // consumer warps
+constexpr int kMaxKu = 12;           // ku per K slice (k-tiles per slice <= 24)
+constexpr int kWaitLimit = 1 << 16;  // tests (<= ~20 us each) before a wait is declared failed
+constexpr int kDrainLimit = 64;      // tests per wait once a failure was seen
 constexpr int kSmemBudget = 110 * 1024;
 
 struct StreamArgs {
@@ -66,6 +66,7 @@ struct StreamArgs {
     int *err;                 // device error word (bit 0: a wait timed out)
     int N, K;
     int nclusters;   // row-block ranges (one cluster each)
+    int sr;          // row blocks per stage (1 or 2)
     int ns;          // ring slots
     int off_steps;   // offset of the steps ring (codes ring at the aligned base)
     int off_x, off_red, off_rbpart;
@@ -73,8 +74,8 @@ struct StreamArgs {
 };
 
 struct StreamMaps {
-    CUtensorMap codes; // uint32 {32, K/256, N}, box {32, K/256/C, 16}, 128-byte swizzle
-    CUtensorMap steps; // uint16 {8, K/256, N},  box {8, K/256/C, 16}
+    CUtensorMap codes; // uint32 {32, K/256, N}, box {32, K/256/C, 16 sr}, 128-byte swizzle
+    CUtensorMap steps; // uint16 {8, K/256, N},  box {8, K/256/C, 16 sr}
 };
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -96,8 +97,8 @@ __device__ __forceinline__ void emit(const StreamArgs &a, int m, int row, float 
     }
 }
 
-template <int MX, bool ARGMAX>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int MX, int KPW, bool ARGMAX>
+__global__ void __launch_bounds__((kMaxWarps + 1) * 32, 2)
 gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -111,20 +112,25 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int W = (int)(blockDim.x >> 5) - 1; // consumer warps; warp W is the producer
+    const int nthreads_c = W * 32;
     const int C = (int)(gridDim.x / a.nclusters);
     const int crank = (C > 1) ? (int)cluster_rank() : 0;
     const int cid = blockIdx.x / C;
     const int nrb = (a.N + 15) >> 4;
     const int nkuc = (a.K >> 8) / C; // ku of this CTA's K slice (C divides K/256)
     const int ku0 = crank * nkuc;
-    const int rb0 = (int)((long long)cid * nrb / a.nclusters);
-    const int nst = (int)((long long)(cid + 1) * nrb / a.nclusters) - rb0; // one stage per row block
-    const int code_slot = nkuc * 2048, step_slot = nkuc * 256;
+    const int sr = a.sr;
+    const int nsb = (nrb + sr - 1) / sr; // stage blocks (sr row blocks each)
+    const int sb0 = (int)((long long)cid * nsb / a.nclusters);
+    const int nst = (int)((long long)(cid + 1) * nsb / a.nclusters) - sb0;
+    const int code_slot = nkuc * 2048 * sr, step_slot = nkuc * 256 * sr;
+    const int red_slot = W * sr * MX * 16; // floats
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.ns; ++i) {
             mbar_init(smem_addr(&full_bar[i]), 1);
-            mbar_init(smem_addr(&empty_bar[i]), kConsumerWarps);
+            mbar_init(smem_addr(&empty_bar[i]), W);
             s_count[i] = 0;
         }
         s_abort = 0;
@@ -137,10 +143,10 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 
     const uint32_t codes_ring = smem_addr(smem);
     const uint32_t steps_ring = codes_ring + a.off_steps;
-    float *red = reinterpret_cast<float *>(smem + a.off_red);       // [ns][8 warps][MX][16]
-    float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart); // [nst][MX][16] (C > 1)
+    float *red = reinterpret_cast<float *>(smem + a.off_red);       // [ns][W][sr][MX][16]
+    float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart); // [nst*sr][MX][16] (C > 1)
 
-    if (warp == kConsumerWarps) {
+    if (warp == W) {
         // ---------------------------------------------------- producer warp
         // Weights do not depend on earlier kernels, so no griddepcontrol.wait.
         if (lane == 0) {
@@ -154,9 +160,10 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                     atomicOr(a.err, 1);
                 }
                 const uint32_t bar = smem_addr(&full_bar[slot]);
+                const int row0 = (sb0 + i) * sr * 16;
                 mbar_arrive_expect_tx(bar, tx);
-                tma_load_3d(codes_ring + slot * code_slot, &maps.codes, 0, ku0, (rb0 + i) * 16, bar, pol);
-                tma_load_3d(steps_ring + slot * step_slot, &maps.steps, 0, ku0, (rb0 + i) * 16, bar, pol);
+                tma_load_3d(codes_ring + slot * code_slot, &maps.codes, 0, ku0, row0, bar, pol);
+                tma_load_3d(steps_ring + slot * step_slot, &maps.steps, 0, ku0, row0, bar, pol);
             }
         }
     } else {
@@ -164,23 +171,29 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         pdl_wait(); // x may be the previous kernel's output
         uint4 *xs = reinterpret_cast<uint4 *>(smem + a.off_x);
         const int cpr = a.K >> 3;
-        for (int i = threadIdx.x; i < MX * cpr; i += kConsumers) {
+        for (int i = threadIdx.x; i < MX * cpr; i += nthreads_c) {
             const int m = i / cpr, c = i - m * cpr;
             xs[i] = permute_x8(*reinterpret_cast<const uint4 *>(a.x + (size_t)m * a.K + c * 8));
         }
         if (threadIdx.x == 0)
             xs[MX * cpr] = make_uint4(0u, 0u, 0u, 0u);
-        named_sync(1, kConsumers);
+        named_sync(1, nthreads_c);
 
         const int g = lane >> 2, t = lane & 3;
+        // B fragments of this warp's k-tiles, held for the whole kernel: lane
+        // (g, t) feeds column g = x-row g>>2 on group slot g&3 (t == g&3), else 0.
         const int bm = g >> 2;
         const bool bsel = ((g & 3) == t) && (bm < MX);
-        const uint4 *xrow = (bsel ? xs + bm * cpr + 4 * t : xs + MX * cpr);
-        const int xstep = bsel ? 16 : 0, xi = bsel ? 1 : 0;
-        const uint4 *xb0 = xrow + xstep * (2 * ku0);
+        uint4 xv[KPW][4];
+#pragma unroll
+        for (int j = 0; j < KPW; ++j) {
+            const int gkt = 2 * ku0 + warp * KPW + j; // k-tile index in the full K
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                xv[j][q] = bsel ? xs[bm * cpr + 16 * gkt + 4 * t + q] : make_uint4(0u, 0u, 0u, 0u);
+        }
         const int ra = (int)((a.perm_lo >> (4 * g)) & 15u);  // weight row of mma row g
         const int rbr = (int)((a.perm_hi >> (4 * g)) & 15u); // weight row of mma row g + 8
-        const int la0 = ra * nkuc, lb0 = rbr * nkuc;         // first 128-byte line of each row
 
         for (int i = 0; i < nst; ++i) {
             const int slot = i % a.ns, use = i / a.ns;
@@ -193,77 +206,68 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
             }
             const uint32_t cb = codes_ring + slot * code_slot;
             const uint32_t sbase = steps_ring + slot * step_slot;
-            float accA = 0.f, accB = 0.f;
-            // 256-k units u = first, first + 8, ...; the rotation balances the
-            // warps over consecutive stages.
-            const int first = (int)((((unsigned)warp + (unsigned)kConsumerWarps * 4096u) - (unsigned)((i * nkuc) % kConsumerWarps)) % (unsigned)kConsumerWarps);
-            for (int u = first; u < nkuc; u += kConsumerWarps) {
-                const int la = la0 + u, lb = lb0 + u;
-                // 16-byte chunk t of k-tile 0 and chunk 4 + t of k-tile 1, swizzled
-                const uint32_t qa0 = cb + la * 128 + ((t ^ (la & 7)) << 4);
-                const uint32_t qb0 = cb + lb * 128 + ((t ^ (lb & 7)) << 4);
-                const uint4 wa0 = lds128(qa0), wa1 = lds128(qa0 ^ 64u);
-                const uint4 wb0 = lds128(qb0), wb1 = lds128(qb0 ^ 64u);
-                const uint32_t pa = sbase + la * 16 + 4 * (t & 1);
-                const uint32_t pb = sbase + lb * 16 + 4 * (t & 1);
-                const uint32_t sa0 = lds32(pa), sa1 = lds32(pa + 8);
-                const uint32_t sb0 = lds32(pb), sb1 = lds32(pb + 8);
-                const uint4 *xb = xb0 + xstep * (2 * u);
-                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint32_t a0w[4] = {wa0.x, wa0.y, wa0.z, wa0.w}, b0w[4] = {wb0.x, wb0.y, wb0.z, wb0.w};
-                const uint32_t a1w[4] = {wa1.x, wa1.y, wa1.z, wa1.w}, b1w[4] = {wb1.x, wb1.y, wb1.z, wb1.w};
+            float *rs = red + slot * red_slot;
+            for (int r = 0; r < sr; ++r) {
+                float accA = 0.f, accB = 0.f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 x0 = xb[xi * q], x1 = xb[xstep + xi * q];
-                    uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
-                    unpack_word(a0w[q], a04, a15, a26, a37);
-                    unpack_word(b0w[q], b04, b15, b26, b37);
-                    mma_16816(c0, a04, b04, a15, b15, x0.x, x0.y);
-                    mma_16816(c0, a26, b26, a37, b37, x0.z, x0.w);
-                    unpack_word(a1w[q], a04, a15, a26, a37);
-                    unpack_word(b1w[q], b04, b15, b26, b37);
-                    mma_16816(c1, a04, b04, a15, b15, x1.x, x1.y);
-                    mma_16816(c1, a26, b26, a37, b37, x1.z, x1.w);
+                for (int j = 0; j < KPW; ++j) {
+                    const int kt = warp * KPW + j; // k-tile within the slice
+                    const int u = kt >> 1;
+                    const int la = (r * 16 + ra) * nkuc + u, lb = (r * 16 + rbr) * nkuc + u;
+                    const int ch = 4 * (kt & 1) + t;
+                    const uint4 wa = lds128(cb + la * 128 + ((ch ^ (la & 7)) << 4));
+                    const uint4 wb = lds128(cb + lb * 128 + ((ch ^ (lb & 7)) << 4));
+                    const uint32_t so = 8 * (kt & 1) + 4 * (t & 1);
+                    const uint32_t sa = lds32(sbase + la * 16 + so);
+                    const uint32_t sb = lds32(sbase + lb * 16 + so);
+                    const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w}, bw[4] = {wb.x, wb.y, wb.z, wb.w};
+                    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+                        unpack_word(aw[q], a04, a15, a26, a37);
+                        unpack_word(bw[q], b04, b15, b26, b37);
+                        // two chains (even / odd words) for instruction-level parallelism
+                        float (&cc)[4] = (q & 1) ? c1 : c0;
+                        mma_16816(cc, a04, b04, a15, b15, xv[j][q].x, xv[j][q].y);
+                        mma_16816(cc, a26, b26, a37, b37, xv[j][q].z, xv[j][q].w);
+                    }
+                    accA = fmaf(bf16lo_to_f32(sa), c0[0] + c1[0], accA);
+                    accA = fmaf(bf16hi_to_f32(sa), c0[1] + c1[1], accA);
+                    accB = fmaf(bf16lo_to_f32(sb), c0[2] + c1[2], accB);
+                    accB = fmaf(bf16hi_to_f32(sb), c0[3] + c1[3], accB);
                 }
-                accA = fmaf(bf16lo_to_f32(sa0), c0[0], accA);
-                accA = fmaf(bf16hi_to_f32(sa0), c0[1], accA);
-                accB = fmaf(bf16lo_to_f32(sb0), c0[2], accB);
-                accB = fmaf(bf16hi_to_f32(sb0), c0[3], accB);
-                accA = fmaf(bf16lo_to_f32(sa1), c1[0], accA);
-                accA = fmaf(bf16hi_to_f32(sa1), c1[1], accA);
-                accB = fmaf(bf16lo_to_f32(sb1), c1[2], accB);
-                accB = fmaf(bf16hi_to_f32(sb1), c1[3], accB);
-            }
-            // This warp's partial of the row block -> red[slot][warp].
-            accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
-            accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
-            const int m = t >> 1;
-            float *rs = red + slot * (kConsumerWarps * MX * 16);
-            if ((t & 1) == 0 && m < MX) {
-                rs[(warp * MX + m) * 16 + ra] = accA;
-                rs[(warp * MX + m) * 16 + rbr] = accB;
+                accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
+                accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+                const int m = t >> 1;
+                if ((t & 1) == 0 && m < MX) {
+                    float *p = rs + ((warp * sr + r) * MX + m) * 16;
+                    p[ra] = accA;
+                    p[rbr] = accB;
+                }
             }
             __syncwarp();
             int last = 0;
             if (lane == 0) {
                 __threadfence_block();
-                last = (atomicAdd(&s_count[slot], 1) == kConsumerWarps - 1);
+                last = (atomicAdd(&s_count[slot], 1) == W - 1);
                 if (last)
                     __threadfence_block();
             }
             last = __shfl_sync(0xFFFFFFFFu, last, 0);
             if (last) {
-                // Sum the warps' partials in warp order; reset the counter
+                // Sum the W warps' partials in warp order; reset the counter
                 // before the slot is released.
-                if (lane < MX * 16) {
-                    float s = 0.f;
-                    for (int w = 0; w < kConsumerWarps; ++w)
-                        s += rs[w * MX * 16 + lane];
-                    const int mm = lane >> 4, rr = lane & 15;
+                for (int e = lane; e < sr * MX * 16; e += 32) {
+                    float v = 0.f;
+                    for (int w = 0; w < W; ++w)
+                        v += rs[w * sr * MX * 16 + e];
+                    const int rr = e & 15, mm = (e >> 4) % MX, r = e / (16 * MX);
+                    const int blk = i * sr + r; // row block within the CTA
                     if (C == 1)
-                        emit(a, mm, (rb0 + i) * 16 + rr, s, s_key, ARGMAX);
+                        emit(a, mm, (sb0 * sr + blk) * 16 + rr, v, s_key, ARGMAX);
                     else
-                        rbpart[i * MX * 16 + lane] = s;
+                        rbpart[(blk * MX + mm) * 16 + rr] = v;
                 }
                 if (lane == 0)
                     s_count[slot] = 0;
@@ -278,16 +282,16 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         // Add the K slices of the cluster's CTAs in rank order through DSMEM;
         // rank r writes elements [r*E/C, (r+1)*E/C) of the cluster's rows.
         cluster_sync();
-        if (warp < kConsumerWarps) {
-            const int E = nst * MX * 16;
+        if (warp < W) {
+            const int E = nst * sr * MX * 16;
             const int e0 = (int)((long long)crank * E / C), e1 = (int)((long long)(crank + 1) * E / C);
             const uint32_t base = smem_addr(rbpart);
-            for (int e = e0 + threadIdx.x; e < e1; e += kConsumers) {
-                float s = 0.f;
+            for (int e = e0 + threadIdx.x; e < e1; e += nthreads_c) {
+                float v = 0.f;
                 for (int c = 0; c < C; ++c)
-                    s += ld_cluster_f32(map_rank(base + 4u * e, (uint32_t)c));
-                const int rr = e & 15, m = (e >> 4) % MX, q = e / (16 * MX);
-                emit(a, m, (rb0 + q) * 16 + rr, s, s_key, ARGMAX);
+                    v += ld_cluster_f32(map_rank(base + 4u * e, (uint32_t)c));
+                const int rr = e & 15, m = (e >> 4) % MX, blk = e / (16 * MX);
+                emit(a, m, (sb0 * sr + blk) * 16 + rr, v, s_key, ARGMAX);
             }
         }
         cluster_sync(); // no CTA leaves while another still reads its shared memory
@@ -305,24 +309,28 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 struct Geometry {
-    int C = 1, nclusters = 1, ns = 1;
+    int C = 1, nclusters = 1, sr = 1, ns = 1, warps = 1, kpw = 1;
     int off_steps = 0, off_x = 0, off_red = 0, off_rbpart = 0, smem = 0;
     bool ok = false;
 };
 
-// Ring for a given split: as many whole-stage slots as the budget allows.
-Geometry make_geometry(int M, int N, int K, int C, int nclusters)
+// Warps and k-tiles per warp for a K slice, and the ring that fits the budget.
+Geometry make_geometry(int M, int N, int K, int C, int nclusters, int sr)
 {
     Geometry G;
     const int nrb = ceil_div(N, 16), nku = K / 256;
     if (nku % C != 0 || nku / C > kMaxKu)
         return G;
     const int nkuc = nku / C;
-    const int max_stages = ceil_div(nrb, nclusters);
-    const int code_slot = nkuc * 2048, step_slot = nkuc * 256;
-    const int red_slot = kConsumerWarps * M * 16 * 4;
+    const int kt = 2 * nkuc;
+    G.kpw = (kt <= kMaxWarps) ? 1 : 2;
+    G.warps = kt / G.kpw;
+    const int nsb = ceil_div(nrb, sr);
+    const int max_stages = ceil_div(nsb, nclusters);
+    const int code_slot = nkuc * 2048 * sr, step_slot = nkuc * 256 * sr;
+    const int red_slot = G.warps * sr * M * 16 * 4;
     const int x_bytes = M * K * 2 + 16;
-    const int rbpart_bytes = (C > 1) ? max_stages * M * 16 * 4 : 0;
+    const int rbpart_bytes = (C > 1) ? max_stages * sr * M * 16 * 4 : 0;
     const int fixed = x_bytes + rbpart_bytes + 1024 + 64;
     int ns = (kSmemBudget - fixed) / (code_slot + step_slot + red_slot);
     if (ns > kMaxSlots)
@@ -333,6 +341,7 @@ Geometry make_geometry(int M, int N, int K, int C, int nclusters)
         return G;
     G.C = C;
     G.nclusters = nclusters;
+    G.sr = sr;
     G.ns = ns;
     G.off_steps = ns * code_slot;
     G.off_x = (G.off_steps + ns * step_slot + 15) & ~15;
@@ -383,7 +392,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, int K, int kus)
+bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, int K, int kus,
+                 int box_rows)
 {
     auto enc = tensor_map_encoder();
     if (!enc)
@@ -393,7 +403,7 @@ bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, i
     {
         cuuint64_t dims[3] = {32, nku, (cuuint64_t)N};
         cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
-        cuuint32_t box[3] = {32, (cuuint32_t)kus, 16};
+        cuuint32_t box[3] = {32, (cuuint32_t)kus, (cuuint32_t)box_rows};
         if (enc(&m.codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -402,7 +412,7 @@ bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, i
     {
         cuuint64_t dims[3] = {8, nku, (cuuint64_t)N};
         cuuint64_t strides[2] = {16, (cuuint64_t)K / 16};
-        cuuint32_t box[3] = {8, (cuuint32_t)kus, 16};
+        cuuint32_t box[3] = {8, (cuuint32_t)kus, (cuuint32_t)box_rows};
         if (enc(&m.steps, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t *>(sc), dims, strides,
                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -411,17 +421,17 @@ bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, i
     return true;
 }
 
-template <int MX, bool ARGMAX>
+template <int MX, int KPW, bool ARGMAX>
 cudaError_t launch_stream(const Geometry &G, const StreamArgs &a, const StreamMaps &maps,
                           cudaStream_t s)
 {
-    auto kern = gemv_stream_kernel<MX, ARGMAX>;
+    auto kern = gemv_stream_kernel<MX, KPW, ARGMAX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G.smem);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G.C * G.nclusters);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3((G.warps + 1) * 32);
     cfg.dynamicSmemBytes = G.smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -436,6 +446,14 @@ cudaError_t launch_stream(const Geometry &G, const StreamArgs &a, const StreamMa
     return cudaLaunchKernelEx(&cfg, kern, a, maps);
 }
 
+template <int MX, bool ARGMAX>
+cudaError_t launch_stream_kpw(const Geometry &G, const StreamArgs &a, const StreamMaps &maps,
+                              cudaStream_t s)
+{
+    return G.kpw == 1 ? launch_stream<MX, 1, ARGMAX>(G, a, maps, s)
+                      : launch_stream<MX, 2, ARGMAX>(G, a, maps, s);
+}
+
 } // namespace
 
 bool stream_supported(int M, int N, int K, const void *qw, const void *sc)
@@ -447,33 +465,40 @@ bool stream_supported(int M, int N, int K, const void *qw, const void *sc)
 
 StreamPlan plan_stream(int M, int N, int K, int num_sms)
 {
-    // Per-shape tiling: cluster size C (K slices, C | K/256, at most 16 ku per
-    // slice) and the number of clusters (16-row blocks split across them), one
-    // CTA per SM. Modelled time of the busiest CTA: its stages, each costing the
-    // larger of the copy engine's per-row cost (~40 cycles per row segment) and
-    // the segment's bytes at ~24 B/cycle.
+    // Per-shape tiling: cluster size C (K slices, C | K/256, at most 12 ku per
+    // slice), stage height sr and the number of clusters, one CTA per SM.
+    // Modelled time of the busiest CTA: its stages, each costing the larger of
+    // the copy engine's per-row cost (~40 cycles per row segment), the segment
+    // bytes at ~24 B/cycle, and the consumers' work (~220 cycles per k-tile per
+    // warp plus ~300 cycles of per-stage overhead).
     StreamPlan best;
     const int nrb = ceil_div(N, 16), nku = K / 256;
     double best_cost = -1.0;
     const int cands[] = {1, 2, 3, 4, 6, 8};
-    for (int C : cands) {
-        if (nku % C != 0 || nku / C > kMaxKu)
-            continue;
-        int ncl = num_sms / C;
-        if (ncl > nrb)
-            ncl = nrb;
-        if (ncl < 1)
-            continue;
-        const Geometry G = make_geometry(M, N, K, C, ncl);
-        if (!G.ok)
-            continue;
-        const double seg = (double)(nku / C) * 128.0;
-        const double per_stage = 16.0 * (seg / 24.0 > 40.0 ? seg / 24.0 : 40.0);
-        const double cost = (double)ceil_div(nrb, ncl) * per_stage;
-        if (best_cost < 0 || cost < best_cost * 0.999) {
-            best_cost = cost;
-            best.C = C;
-            best.nclusters = ncl;
+    for (int sr = 1; sr <= 2; ++sr) {
+        const int nsb = ceil_div(nrb, sr);
+        for (int C : cands) {
+            if (nku % C != 0 || nku / C > kMaxKu)
+                continue;
+            int ncl = num_sms / C;
+            if (ncl > nsb)
+                ncl = nsb;
+            if (ncl < 1)
+                continue;
+            const Geometry G = make_geometry(M, N, K, C, ncl, sr);
+            if (!G.ok)
+                continue;
+            const double seg = (double)(nku / C) * 128.0;
+            const double copy = 16.0 * sr * (seg / 24.0 > 40.0 ? seg / 24.0 : 40.0);
+            const double work = 300.0 + 220.0 * G.kpw * sr;
+            const double per_stage = copy > work ? copy : work;
+            const double cost = (double)ceil_div(nsb, ncl) * per_stage;
+            if (best_cost < 0 || cost < best_cost * 0.999) {
+                best_cost = cost;
+                best.C = C;
+                best.nclusters = ncl;
+                best.sr = sr;
+            }
         }
     }
     best.ok = best_cost >= 0;
@@ -484,12 +509,12 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
                        const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
                        int32_t *argmax, int *err, cudaStream_t s)
 {
-    const Geometry G = make_geometry(M, N, K, p.C, p.nclusters);
+    const Geometry G = make_geometry(M, N, K, p.C, p.nclusters, p.sr);
     if (!G.ok)
         return cudaErrorInvalidConfiguration;
     const int nkuc = (K / 256) / G.C;
     StreamMaps maps;
-    if (!encode_maps(maps, qw, sc, N, K, nkuc))
+    if (!encode_maps(maps, qw, sc, N, K, nkuc, 16 * G.sr))
         return cudaErrorInvalidValue;
     StreamArgs a;
     a.y = y;
@@ -499,6 +524,7 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
     a.N = N;
     a.K = K;
     a.nclusters = G.nclusters;
+    a.sr = G.sr;
     a.ns = G.ns;
     a.off_steps = G.off_steps;
     a.off_x = G.off_x;
@@ -508,9 +534,9 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
     const bool am = argmax != nullptr;
     cudaError_t e;
     if (M == 1)
-        e = am ? launch_stream<1, true>(G, a, maps, s) : launch_stream<1, false>(G, a, maps, s);
+        e = am ? launch_stream_kpw<1, true>(G, a, maps, s) : launch_stream_kpw<1, false>(G, a, maps, s);
     else
-        e = am ? launch_stream<2, true>(G, a, maps, s) : launch_stream<2, false>(G, a, maps, s);
+        e = am ? launch_stream_kpw<2, true>(G, a, maps, s) : launch_stream_kpw<2, false>(G, a, maps, s);
     if (e != cudaSuccess || !am)
         return e;
     return run_argmax_finalize(argmax, keys, M, G.C * G.nclusters, s);

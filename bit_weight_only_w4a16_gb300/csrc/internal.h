@@ -29,6 +29,7 @@ cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const u
 struct StreamPlan {
     int C = 1;
     int nclusters = 1;
+    int sr = 1; // 16-row blocks per stage
     bool ok = false;
 };
 
