@@ -27,14 +27,16 @@
 // every row a contiguous run of K-slice/2 bytes, which is what the copy engine
 // streams fastest) and one of steps. Consumer warp w owns the fixed k-tiles
 // w*KPW .. w*KPW + KPW - 1 of the slice (W * KPW = k-tiles per slice), so its
-// B fragments (x) are loaded into registers once per kernel and each stage
-// costs it only two 128-bit and two 32-bit shared loads per k-tile. Every warp
-// reads every stage, so slots are consumed and refilled in order and the whole
-// ring stays in flight; the last warp to finish a stage adds the W partials in
-// warp order. Codes land with the hardware's 128-byte swizzle (16-byte chunk c
-// of line L at chunk c ^ (L & 7)); the mma row -> weight row map pairs rows
-// whose lines differ in bit 2 of L & 7, so each 8-lane phase of a 128-bit read
-// touches all 32 banks once. Steps arrive as [row][ku][8 x bf16], unswizzled.
+// B fragments (x) and its shared-memory offsets are set up once per kernel and
+// each stage costs it two 128-bit and two 32-bit shared loads per k-tile plus
+// one mbarrier wait and one arrive. Every warp reads every stage, so slots are
+// consumed and refilled in order and the whole ring stays in flight. The
+// producer warp, idle between copies, adds the W partials of each finished
+// stage in warp order before refilling its slot. Codes land with the
+// hardware's 128-byte swizzle (16-byte chunk c of line L at chunk c ^ (L & 7));
+// the mma row -> weight row map pairs rows whose lines differ in bit 2 of
+// L & 7, so each 8-lane phase of a 128-bit read touches all 32 banks once.
+// Steps arrive as [row][ku][8 x bf16], unswizzled.
 //
 // Inner product: exact (code - 8) bf16 x bf16 m16n8k16 mma with fp32 accumulate.
 // Lane (g, t) holds group 4*kt + t of two weight rows; B column 4*m + s carries
@@ -66,7 +68,6 @@ struct StreamArgs {
     int *err;                 // device error word (bit 0: a wait timed out)
     int N, K;
     int nclusters;   // row-block ranges (one cluster each)
-    int sr;          // row blocks per stage (1 or 2)
     int ns;          // ring slots
     int off_steps;   // offset of the steps ring (codes ring at the aligned base)
     int off_x, off_red, off_rbpart;
@@ -97,14 +98,13 @@ __device__ __forceinline__ void emit(const StreamArgs &a, int m, int row, float 
     }
 }
 
-template <int MX, int KPW, bool ARGMAX>
+template <int MX, int KPW, int SR, bool ARGMAX>
 __global__ void __launch_bounds__((kMaxWarps + 1) * 32, 2)
 gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) unsigned long long full_bar[kMaxSlots];
     __shared__ __align__(8) unsigned long long empty_bar[kMaxSlots];
-    __shared__ int s_count[kMaxSlots];
     __shared__ int s_abort;
     __shared__ unsigned long long s_key[MX];
 
@@ -120,18 +120,17 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
     const int nrb = (a.N + 15) >> 4;
     const int nkuc = (a.K >> 8) / C; // ku of this CTA's K slice (C divides K/256)
     const int ku0 = crank * nkuc;
-    const int sr = a.sr;
-    const int nsb = (nrb + sr - 1) / sr; // stage blocks (sr row blocks each)
+    const int nsb = (nrb + SR - 1) / SR; // stage blocks (SR row blocks each)
     const int sb0 = (int)((long long)cid * nsb / a.nclusters);
     const int nst = (int)((long long)(cid + 1) * nsb / a.nclusters) - sb0;
-    const int code_slot = nkuc * 2048 * sr, step_slot = nkuc * 256 * sr;
-    const int red_slot = W * sr * MX * 16; // floats
+    const int ns = a.ns;
+    const uint32_t code_slot = (uint32_t)(nkuc * 2048 * SR), step_slot = (uint32_t)(nkuc * 256 * SR);
+    constexpr int kElems = SR * MX * 16; // outputs of one stage
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < a.ns; ++i) {
+        for (int i = 0; i < ns; ++i) {
             mbar_init(smem_addr(&full_bar[i]), 1);
             mbar_init(smem_addr(&empty_bar[i]), W);
-            s_count[i] = 0;
         }
         s_abort = 0;
         fence_mbar_init();
@@ -143,28 +142,69 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 
     const uint32_t codes_ring = smem_addr(smem);
     const uint32_t steps_ring = codes_ring + a.off_steps;
-    float *red = reinterpret_cast<float *>(smem + a.off_red);       // [ns][W][sr][MX][16]
-    float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart); // [nst*sr][MX][16] (C > 1)
+    float *red = reinterpret_cast<float *>(smem + a.off_red);       // [ns][W][kElems]
+    float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart); // [nst][kElems] (C > 1)
 
     if (warp == W) {
         // ---------------------------------------------------- producer warp
         // Weights do not depend on earlier kernels, so no griddepcontrol.wait.
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            const uint32_t tx = (uint32_t)(code_slot + step_slot);
-            for (int i = 0; i < nst; ++i) {
-                const int slot = i % a.ns, use = i / a.ns;
-                if (use > 0 && !mbar_wait_bounded(smem_addr(&empty_bar[slot]), (use - 1) & 1,
-                                                  s_abort ? kDrainLimit : kWaitLimit)) {
+        // Adds up stage j's W partials once its slot is released, then refills.
+        const uint64_t pol = policy_evict_first();
+        const uint32_t tx = code_slot + step_slot;
+        auto reduce_stage = [&](int j, int slot) {
+            const float *rs = red + slot * (W * kElems);
+            for (int e = lane; e < kElems; e += 32) {
+                float v = 0.f;
+                for (int w = 0; w < W; ++w)
+                    v += rs[w * kElems + e];
+                const int rr = e & 15, m = (e >> 4) % MX, r = e / (16 * MX);
+                const int blk = j * SR + r; // row block within the CTA
+                if (C == 1)
+                    emit(a, m, (sb0 * SR + blk) * 16 + rr, v, s_key, ARGMAX);
+                else
+                    rbpart[(blk * MX + m) * 16 + rr] = v;
+            }
+        };
+        int slot = 0, use = 0;
+        for (int i = 0; i < nst; ++i) {
+            if (use > 0) {
+                int ok = 1;
+                if (lane == 0)
+                    ok = mbar_wait_bounded(smem_addr(&empty_bar[slot]), (use - 1) & 1,
+                                           s_abort ? kDrainLimit : kWaitLimit);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok && lane == 0) {
                     s_abort = 1;
                     atomicOr(a.err, 1);
                 }
+                reduce_stage(i - ns, slot);
+                __syncwarp();
+            }
+            if (lane == 0) {
                 const uint32_t bar = smem_addr(&full_bar[slot]);
-                const int row0 = (sb0 + i) * sr * 16;
+                const int row0 = (sb0 + i) * SR * 16;
                 mbar_arrive_expect_tx(bar, tx);
                 tma_load_3d(codes_ring + slot * code_slot, &maps.codes, 0, ku0, row0, bar, pol);
                 tma_load_3d(steps_ring + slot * step_slot, &maps.steps, 0, ku0, row0, bar, pol);
             }
+            if (++slot == ns) {
+                slot = 0;
+                ++use;
+            }
+        }
+        // The last min(ns, nst) stages: wait for their release, then add them up.
+        for (int j = nst - ns > 0 ? nst - ns : 0; j < nst; ++j) {
+            const int sl = j % ns, u = j / ns;
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait_bounded(smem_addr(&empty_bar[sl]), u & 1,
+                                       s_abort ? kDrainLimit : kWaitLimit);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok && lane == 0) {
+                s_abort = 1;
+                atomicOr(a.err, 1);
+            }
+            reduce_stage(j, sl);
         }
     } else {
         // -------------------------------------------------- consumer warps
@@ -192,34 +232,48 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
             for (int q = 0; q < 4; ++q)
                 xv[j][q] = bsel ? xs[bm * cpr + 16 * gkt + 4 * t + q] : make_uint4(0u, 0u, 0u, 0u);
         }
+        // Byte offsets inside a slot of this lane's codes and steps, per row block
+        // of the stage and per owned k-tile (constant for the whole kernel).
         const int ra = (int)((a.perm_lo >> (4 * g)) & 15u);  // weight row of mma row g
         const int rbr = (int)((a.perm_hi >> (4 * g)) & 15u); // weight row of mma row g + 8
+        uint32_t qoa[SR][KPW], qob[SR][KPW], soa[SR][KPW], sob[SR][KPW];
+#pragma unroll
+        for (int r = 0; r < SR; ++r) {
+#pragma unroll
+            for (int j = 0; j < KPW; ++j) {
+                const int kt = warp * KPW + j, u = kt >> 1, ch = 4 * (kt & 1) + t;
+                const int la = (r * 16 + ra) * nkuc + u, lb = (r * 16 + rbr) * nkuc + u;
+                qoa[r][j] = la * 128 + ((ch ^ (la & 7)) << 4);
+                qob[r][j] = lb * 128 + ((ch ^ (lb & 7)) << 4);
+                soa[r][j] = la * 16 + 8 * (kt & 1) + 4 * (t & 1);
+                sob[r][j] = lb * 16 + 8 * (kt & 1) + 4 * (t & 1);
+            }
+        }
+        const int m = t >> 1;
+        const bool writer = ((t & 1) == 0) && (m < MX);
+        float *my_red = red + warp * kElems + m * 16;
 
+        uint32_t cb = codes_ring, sbase = steps_ring;
+        float *rs = my_red;
+        int slot = 0;
+        uint32_t phase = 0;
         for (int i = 0; i < nst; ++i) {
-            const int slot = i % a.ns, use = i / a.ns;
-            if (!mbar_wait_bounded(smem_addr(&full_bar[slot]), use & 1,
+            if (!mbar_wait_bounded(smem_addr(&full_bar[slot]), phase,
                                    s_abort ? kDrainLimit : kWaitLimit)) {
                 if (lane == 0) {
                     s_abort = 1;
                     atomicOr(a.err, 1);
                 }
             }
-            const uint32_t cb = codes_ring + slot * code_slot;
-            const uint32_t sbase = steps_ring + slot * step_slot;
-            float *rs = red + slot * red_slot;
-            for (int r = 0; r < sr; ++r) {
+#pragma unroll
+            for (int r = 0; r < SR; ++r) {
                 float accA = 0.f, accB = 0.f;
 #pragma unroll
                 for (int j = 0; j < KPW; ++j) {
-                    const int kt = warp * KPW + j; // k-tile within the slice
-                    const int u = kt >> 1;
-                    const int la = (r * 16 + ra) * nkuc + u, lb = (r * 16 + rbr) * nkuc + u;
-                    const int ch = 4 * (kt & 1) + t;
-                    const uint4 wa = lds128(cb + la * 128 + ((ch ^ (la & 7)) << 4));
-                    const uint4 wb = lds128(cb + lb * 128 + ((ch ^ (lb & 7)) << 4));
-                    const uint32_t so = 8 * (kt & 1) + 4 * (t & 1);
-                    const uint32_t sa = lds32(sbase + la * 16 + so);
-                    const uint32_t sb = lds32(sbase + lb * 16 + so);
+                    const uint4 wa = lds128(cb + qoa[r][j]);
+                    const uint4 wb = lds128(cb + qob[r][j]);
+                    const uint32_t sa = lds32(sbase + soa[r][j]);
+                    const uint32_t sb = lds32(sbase + sob[r][j]);
                     const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w}, bw[4] = {wb.x, wb.y, wb.z, wb.w};
                     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -239,42 +293,25 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                 }
                 accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
                 accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
-                const int m = t >> 1;
-                if ((t & 1) == 0 && m < MX) {
-                    float *p = rs + ((warp * sr + r) * MX + m) * 16;
-                    p[ra] = accA;
-                    p[rbr] = accB;
+                if (writer) {
+                    rs[r * MX * 16 + ra] = accA;
+                    rs[r * MX * 16 + rbr] = accB;
                 }
             }
             __syncwarp();
-            int last = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                last = (atomicAdd(&s_count[slot], 1) == W - 1);
-                if (last)
-                    __threadfence_block();
-            }
-            last = __shfl_sync(0xFFFFFFFFu, last, 0);
-            if (last) {
-                // Sum the W warps' partials in warp order; reset the counter
-                // before the slot is released.
-                for (int e = lane; e < sr * MX * 16; e += 32) {
-                    float v = 0.f;
-                    for (int w = 0; w < W; ++w)
-                        v += rs[w * sr * MX * 16 + e];
-                    const int rr = e & 15, mm = (e >> 4) % MX, r = e / (16 * MX);
-                    const int blk = i * sr + r; // row block within the CTA
-                    if (C == 1)
-                        emit(a, mm, (sb0 * sr + blk) * 16 + rr, v, s_key, ARGMAX);
-                    else
-                        rbpart[(blk * MX + mm) * 16 + rr] = v;
-                }
-                if (lane == 0)
-                    s_count[slot] = 0;
-                __syncwarp();
-            }
             if (lane == 0)
                 mbar_arrive(smem_addr(&empty_bar[slot]));
+            if (++slot == ns) {
+                slot = 0;
+                phase ^= 1u;
+                cb = codes_ring;
+                sbase = steps_ring;
+                rs = my_red;
+            } else {
+                cb += code_slot;
+                sbase += step_slot;
+                rs += W * kElems;
+            }
         }
     }
 
@@ -283,15 +320,15 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         // rank r writes elements [r*E/C, (r+1)*E/C) of the cluster's rows.
         cluster_sync();
         if (warp < W) {
-            const int E = nst * sr * MX * 16;
+            const int E = nst * kElems;
             const int e0 = (int)((long long)crank * E / C), e1 = (int)((long long)(crank + 1) * E / C);
             const uint32_t base = smem_addr(rbpart);
             for (int e = e0 + threadIdx.x; e < e1; e += nthreads_c) {
                 float v = 0.f;
                 for (int c = 0; c < C; ++c)
                     v += ld_cluster_f32(map_rank(base + 4u * e, (uint32_t)c));
-                const int rr = e & 15, m = (e >> 4) % MX, blk = e / (16 * MX);
-                emit(a, m, (sb0 * sr + blk) * 16 + rr, v, s_key, ARGMAX);
+                const int rr = e & 15, mm = (e >> 4) % MX, blk = e / (16 * MX);
+                emit(a, mm, (sb0 * SR + blk) * 16 + rr, v, s_key, ARGMAX);
             }
         }
         cluster_sync(); // no CTA leaves while another still reads its shared memory
@@ -325,6 +362,8 @@ Geometry make_geometry(int M, int N, int K, int C, int nclusters, int sr)
     const int kt = 2 * nkuc;
     G.kpw = (kt <= kMaxWarps) ? 1 : 2;
     G.warps = kt / G.kpw;
+    if (G.kpw == 2 && sr == 2)
+        return G; // register budget: two k-tiles per warp only with one-block stages
     const int nsb = ceil_div(nrb, sr);
     const int max_stages = ceil_div(nsb, nclusters);
     const int code_slot = nkuc * 2048 * sr, step_slot = nkuc * 256 * sr;
@@ -421,11 +460,11 @@ bool encode_maps(StreamMaps &m, const uint32_t *qw, const uint16_t *sc, int N, i
     return true;
 }
 
-template <int MX, int KPW, bool ARGMAX>
+template <int MX, int KPW, int SR, bool ARGMAX>
 cudaError_t launch_stream(const Geometry &G, const StreamArgs &a, const StreamMaps &maps,
                           cudaStream_t s)
 {
-    auto kern = gemv_stream_kernel<MX, KPW, ARGMAX>;
+    auto kern = gemv_stream_kernel<MX, KPW, SR, ARGMAX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G.smem);
     if (e != cudaSuccess)
         return e;
@@ -450,8 +489,10 @@ template <int MX, bool ARGMAX>
 cudaError_t launch_stream_kpw(const Geometry &G, const StreamArgs &a, const StreamMaps &maps,
                               cudaStream_t s)
 {
-    return G.kpw == 1 ? launch_stream<MX, 1, ARGMAX>(G, a, maps, s)
-                      : launch_stream<MX, 2, ARGMAX>(G, a, maps, s);
+    if (G.sr == 2)
+        return launch_stream<MX, 1, 2, ARGMAX>(G, a, maps, s);
+    return G.kpw == 1 ? launch_stream<MX, 1, 1, ARGMAX>(G, a, maps, s)
+                      : launch_stream<MX, 2, 1, ARGMAX>(G, a, maps, s);
 }
 
 } // namespace
@@ -524,7 +565,6 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
     a.N = N;
     a.K = K;
     a.nclusters = G.nclusters;
-    a.sr = G.sr;
     a.ns = G.ns;
     a.off_steps = G.off_steps;
     a.off_x = G.off_x;
