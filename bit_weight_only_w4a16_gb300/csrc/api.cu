@@ -5,6 +5,7 @@
 #include "internal.h"
 
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -22,6 +23,23 @@ struct DeviceState {
 };
 
 DeviceState g_dev[kMaxDevices];
+
+// Decode kernel selection: W4_DECODE_PATH=stream | register forces one of the
+// two decode kernels (both compute the full result; used by the tests and the
+// per-shape tuning sweep). Unset or anything else: the per-shape table.
+enum DecodePath { kPathAuto = 0, kPathStream = 1, kPathRegister = 2 };
+DecodePath decode_path()
+{
+    static const DecodePath p = [] {
+        const char *e = std::getenv("W4_DECODE_PATH");
+        if (e && std::strcmp(e, "stream") == 0)
+            return kPathStream;
+        if (e && std::strcmp(e, "register") == 0)
+            return kPathRegister;
+        return kPathAuto;
+    }();
+    return p;
+}
 std::mutex g_mu;
 thread_local char g_cuda_err[256] = "";
 
@@ -109,6 +127,19 @@ bool decode_fits(const w4::DecodePlan &p, int M, int K)
     return smem <= 220 * 1024;
 }
 
+// Which decode kernel serves (M, N, K): the tensor-copy streaming kernel where
+// it measured faster on GB300, the register-streaming kernel otherwise.
+bool use_stream(int M, int N, int K, const void *qw, const void *sc)
+{
+    if (!w4::stream_supported(M, N, K, qw, sc))
+        return false;
+    switch (decode_path()) {
+    case kPathStream: return true;
+    case kPathRegister: return false;
+    default: return w4::stream_preferred(M, N, K);
+    }
+}
+
 } // namespace
 
 extern "C" {
@@ -146,7 +177,7 @@ int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (w4::stream_supported(M, N, K, qweight, scales)) {
+    if (use_stream(M, N, K, qweight, scales)) {
         const w4::StreamPlan sp = w4::plan_stream(M, N, K, st->num_sms);
         if (sp.ok) {
             cudaError_t e = w4::run_stream(sp, y, x, qweight, scales, M, N, K, nullptr, nullptr,
@@ -197,7 +228,7 @@ int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (w4::stream_supported(M, N, K, qweight, scales)) {
+    if (use_stream(M, N, K, qweight, scales)) {
         const w4::StreamPlan sp = w4::plan_stream(M, N, K, st->num_sms);
         if (sp.ok && (size_t)M * sp.C * sp.nclusters <= kKeyCapacity) {
             cudaError_t e = w4::run_stream(sp, y, x, qweight, scales, M, N, K, st->keys, argmax,

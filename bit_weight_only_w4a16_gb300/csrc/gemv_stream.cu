@@ -60,6 +60,10 @@ constexpr int kMaxKu = 12;           // ku per K slice (k-tiles per slice <= 24)
 constexpr int kWaitLimit = 1 << 16;  // tests (<= ~20 us each) before a wait is declared failed
 constexpr int kDrainLimit = 64;      // tests per wait once a failure was seen
 constexpr int kSmemBudget = 110 * 1024;
+// Stages issued before the previous kernel has finished. The copy engine is
+// shared with that kernel's CTA on the same SM, so a deeper early prefetch
+// would queue ahead of (and delay) its refills.
+constexpr int kPreStages = 3;
 
 struct StreamArgs {
     float *y;
@@ -105,6 +109,7 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) unsigned long long full_bar[kMaxSlots];
     __shared__ __align__(8) unsigned long long empty_bar[kMaxSlots];
+    __shared__ __align__(8) unsigned long long done_bar[2 * kMaxSlots];
     __shared__ int s_abort;
     __shared__ unsigned long long s_key[MX];
 
@@ -132,6 +137,8 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
             mbar_init(smem_addr(&full_bar[i]), 1);
             mbar_init(smem_addr(&empty_bar[i]), W);
         }
+        for (int i = 0; i < 2 * ns; ++i)
+            mbar_init(smem_addr(&done_bar[i]), W);
         s_abort = 0;
         fence_mbar_init();
     }
@@ -142,7 +149,7 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
 
     const uint32_t codes_ring = smem_addr(smem);
     const uint32_t steps_ring = codes_ring + a.off_steps;
-    float *red = reinterpret_cast<float *>(smem + a.off_red);       // [ns][W][kElems]
+    float *red = reinterpret_cast<float *>(smem + a.off_red);       // [2 ns][W][kElems]
     float *rbpart = reinterpret_cast<float *>(smem + a.off_rbpart); // [nst][kElems] (C > 1)
 
     if (warp == W) {
@@ -151,8 +158,18 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         // Adds up stage j's W partials once its slot is released, then refills.
         const uint64_t pol = policy_evict_first();
         const uint32_t tx = code_slot + step_slot;
-        auto reduce_stage = [&](int j, int slot) {
-            const float *rs = red + slot * (W * kElems);
+        auto reduce_stage = [&](int j) {
+            // Stage j's partials are in red slot j % (2 ns) once done_bar says so.
+            const int rsl = j % (2 * ns), u = j / (2 * ns);
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait_bounded(smem_addr(&done_bar[rsl]), u & 1, s_abort ? kDrainLimit : kWaitLimit);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok && lane == 0) {
+                s_abort = 1;
+                atomicOr(a.err, 1);
+            }
+            const float *rs = red + rsl * (W * kElems);
             for (int e = lane; e < kElems; e += 32) {
                 float v = 0.f;
                 for (int w = 0; w < W; ++w)
@@ -164,10 +181,14 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                 else
                     rbpart[(blk * MX + m) * 16 + rr] = v;
             }
+            __syncwarp();
         };
         int slot = 0, use = 0;
         for (int i = 0; i < nst; ++i) {
+            if (i == kPreStages)
+                pdl_wait();
             if (use > 0) {
+                // Slot reuse: its previous stage (i - ns) has been read out.
                 int ok = 1;
                 if (lane == 0)
                     ok = mbar_wait_bounded(smem_addr(&empty_bar[slot]), (use - 1) & 1,
@@ -177,8 +198,6 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                     s_abort = 1;
                     atomicOr(a.err, 1);
                 }
-                reduce_stage(i - ns, slot);
-                __syncwarp();
             }
             if (lane == 0) {
                 const uint32_t bar = smem_addr(&full_bar[slot]);
@@ -187,27 +206,24 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                 tma_load_3d(codes_ring + slot * code_slot, &maps.codes, 0, ku0, row0, bar, pol);
                 tma_load_3d(steps_ring + slot * step_slot, &maps.steps, 0, ku0, row0, bar, pol);
             }
+            __syncwarp();
+            // Partials of stage i - ns must be added before stage i + ns can
+            // write the same red slot; stage i + ns cannot be issued earlier.
+            if (i >= ns)
+                reduce_stage(i - ns);
             if (++slot == ns) {
                 slot = 0;
                 ++use;
             }
         }
-        // The last min(ns, nst) stages: wait for their release, then add them up.
-        for (int j = nst - ns > 0 ? nst - ns : 0; j < nst; ++j) {
-            const int sl = j % ns, u = j / ns;
-            int ok = 1;
-            if (lane == 0)
-                ok = mbar_wait_bounded(smem_addr(&empty_bar[sl]), u & 1,
-                                       s_abort ? kDrainLimit : kWaitLimit);
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            if (!ok && lane == 0) {
-                s_abort = 1;
-                atomicOr(a.err, 1);
-            }
-            reduce_stage(j, sl);
-        }
+        for (int j = nst - ns > 0 ? nst - ns : 0; j < nst; ++j)
+            reduce_stage(j);
     } else {
         // -------------------------------------------------- consumer warps
+        // Warm L2 with x while the previous kernel runs (a prefetch never
+        // returns data, so it cannot observe a value the wait must order).
+        for (int off = threadIdx.x * 128; off < MX * a.K * 2; off += nthreads_c * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char *>(a.x) + off));
         pdl_wait(); // x may be the previous kernel's output
         uint4 *xs = reinterpret_cast<uint4 *>(smem + a.off_x);
         const int cpr = a.K >> 3;
@@ -254,9 +270,8 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
         float *my_red = red + warp * kElems + m * 16;
 
         uint32_t cb = codes_ring, sbase = steps_ring;
-        float *rs = my_red;
-        int slot = 0;
-        uint32_t phase = 0;
+        int slot = 0, rslot = 0;
+        uint32_t phase = 0, rphase = 0;
         for (int i = 0; i < nst; ++i) {
             if (!mbar_wait_bounded(smem_addr(&full_bar[slot]), phase,
                                    s_abort ? kDrainLimit : kWaitLimit)) {
@@ -265,16 +280,31 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                     atomicOr(a.err, 1);
                 }
             }
+            // Copy this warp's part of the stage to registers and release the
+            // slot at once, so the refill overlaps the arithmetic.
+            uint4 wa[SR][KPW], wb[SR][KPW];
+            uint32_t sa[SR][KPW], sb[SR][KPW];
+#pragma unroll
+            for (int r = 0; r < SR; ++r) {
+#pragma unroll
+                for (int j = 0; j < KPW; ++j) {
+                    wa[r][j] = lds128(cb + qoa[r][j]);
+                    wb[r][j] = lds128(cb + qob[r][j]);
+                    sa[r][j] = lds32(sbase + soa[r][j]);
+                    sb[r][j] = lds32(sbase + sob[r][j]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&empty_bar[slot]));
+            float *rs = my_red + rslot * (W * kElems);
 #pragma unroll
             for (int r = 0; r < SR; ++r) {
                 float accA = 0.f, accB = 0.f;
 #pragma unroll
                 for (int j = 0; j < KPW; ++j) {
-                    const uint4 wa = lds128(cb + qoa[r][j]);
-                    const uint4 wb = lds128(cb + qob[r][j]);
-                    const uint32_t sa = lds32(sbase + soa[r][j]);
-                    const uint32_t sb = lds32(sbase + sob[r][j]);
-                    const uint32_t aw[4] = {wa.x, wa.y, wa.z, wa.w}, bw[4] = {wb.x, wb.y, wb.z, wb.w};
+                    const uint32_t aw[4] = {wa[r][j].x, wa[r][j].y, wa[r][j].z, wa[r][j].w};
+                    const uint32_t bw[4] = {wb[r][j].x, wb[r][j].y, wb[r][j].z, wb[r][j].w};
                     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -286,10 +316,10 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
                         mma_16816(cc, a04, b04, a15, b15, xv[j][q].x, xv[j][q].y);
                         mma_16816(cc, a26, b26, a37, b37, xv[j][q].z, xv[j][q].w);
                     }
-                    accA = fmaf(bf16lo_to_f32(sa), c0[0] + c1[0], accA);
-                    accA = fmaf(bf16hi_to_f32(sa), c0[1] + c1[1], accA);
-                    accB = fmaf(bf16lo_to_f32(sb), c0[2] + c1[2], accB);
-                    accB = fmaf(bf16hi_to_f32(sb), c0[3] + c1[3], accB);
+                    accA = fmaf(bf16lo_to_f32(sa[r][j]), c0[0] + c1[0], accA);
+                    accA = fmaf(bf16hi_to_f32(sa[r][j]), c0[1] + c1[1], accA);
+                    accB = fmaf(bf16lo_to_f32(sb[r][j]), c0[2] + c1[2], accB);
+                    accB = fmaf(bf16hi_to_f32(sb[r][j]), c0[3] + c1[3], accB);
                 }
                 accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
                 accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
@@ -300,19 +330,22 @@ gemv_stream_kernel(const StreamArgs a, const __grid_constant__ StreamMaps maps)
             }
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(smem_addr(&empty_bar[slot]));
+                mbar_arrive(smem_addr(&done_bar[rslot]));
             if (++slot == ns) {
                 slot = 0;
                 phase ^= 1u;
                 cb = codes_ring;
                 sbase = steps_ring;
-                rs = my_red;
             } else {
                 cb += code_slot;
                 sbase += step_slot;
-                rs += W * kElems;
+            }
+            if (++rslot == 2 * ns) {
+                rslot = 0;
+                rphase ^= 1u;
             }
         }
+        (void)rphase;
     }
 
     if (C > 1) {
@@ -371,7 +404,7 @@ Geometry make_geometry(int M, int N, int K, int C, int nclusters, int sr)
     const int x_bytes = M * K * 2 + 16;
     const int rbpart_bytes = (C > 1) ? max_stages * sr * M * 16 * 4 : 0;
     const int fixed = x_bytes + rbpart_bytes + 1024 + 64;
-    int ns = (kSmemBudget - fixed) / (code_slot + step_slot + red_slot);
+    int ns = (kSmemBudget - fixed) / (code_slot + step_slot + 2 * red_slot);
     if (ns > kMaxSlots)
         ns = kMaxSlots;
     if (ns > max_stages)
@@ -385,7 +418,7 @@ Geometry make_geometry(int M, int N, int K, int C, int nclusters, int sr)
     G.off_steps = ns * code_slot;
     G.off_x = (G.off_steps + ns * step_slot + 15) & ~15;
     G.off_red = (G.off_x + x_bytes + 15) & ~15;
-    G.off_rbpart = (G.off_red + ns * red_slot + 15) & ~15;
+    G.off_rbpart = (G.off_red + 2 * ns * red_slot + 15) & ~15;
     G.smem = G.off_rbpart + rbpart_bytes + 1024; // + alignment slack
     G.ok = true;
     return G;
@@ -502,6 +535,13 @@ bool stream_supported(int M, int N, int K, const void *qw, const void *sc)
     (void)N;
     return M >= 1 && M <= 2 && K % 256 == 0 && (reinterpret_cast<uintptr_t>(qw) & 15) == 0 &&
            (reinterpret_cast<uintptr_t>(sc) & 15) == 0 && tensor_map_encoder() != nullptr;
+}
+
+bool stream_preferred(int M, int N, int K)
+{
+    // Measured per-shape winner; refreshed by the tuning sweep.
+    (void)M;
+    return (long long)N * K >= (long long)12288 * 1536 && K <= 1536;
 }
 
 StreamPlan plan_stream(int M, int N, int K, int num_sms)

@@ -34,6 +34,8 @@ struct StreamPlan {
 };
 
 bool stream_supported(int M, int N, int K, const void *qw, const void *sc);
+// Per-shape choice between the two decode kernels (from measurements on GB300).
+bool stream_preferred(int M, int N, int K);
 StreamPlan plan_stream(int M, int N, int K, int num_sms);
 cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                        const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
