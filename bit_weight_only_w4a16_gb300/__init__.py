@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED",
 
 # Symbols declared in include/w4a16.h.
 EXPORTS = ("w4_status_string", "w4_last_cuda_error", "w4_init", "w4_device_error", "w4a16_gemv", "w4a16_gemm",
-           "w4a16_gemv_argmax", "w4_embed_gather", "hbm_read_probe")
+           "w4a16_gemv_argmax", "w4a16_gemv_argmax_noalloc", "w4_embed_gather", "hbm_read_probe")
 
 
 class W4Error(RuntimeError):
@@ -52,8 +52,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.argtypes = [P, P, P, P, I, I, I, I, P]
         f.restype = I
-    lib.w4a16_gemv_argmax.argtypes = [P, P, P, P, P, I, I, I, I, P]
-    lib.w4a16_gemv_argmax.restype = I
+    for name in ("w4a16_gemv_argmax", "w4a16_gemv_argmax_noalloc"):
+        f = getattr(lib, name)
+        f.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        f.restype = I
     lib.w4_embed_gather.argtypes = [P, P, P, P, I, I, I, I, P, P]
     lib.w4_embed_gather.restype = I
     lib.hbm_read_probe.argtypes = [P, P, S, P]
@@ -150,6 +152,19 @@ def w4a16_gemv_argmax(x, qweight, scales, group: int = 32, out=None, argmax=None
     a = torch.empty((M,), dtype=torch.int32, device=x.device) if argmax is None else _cuda(argmax, "argmax")
     _check(_lib.w4a16_gemv_argmax(_ptr(y), _ptr(a), _ptr(x), _ptr(qweight), _ptr(scales), M, N, K,
                                   group, _stream(stream)), "w4a16_gemv_argmax")
+    return y, a
+
+
+def w4a16_gemv_argmax_noalloc(x, qweight, scales, group: int = 32, out=None, argmax=None, stream=None):
+    """w4a16_gemv_argmax whose library scratch is a fixed device array (no device
+    allocation inside the call; y and argmax are allocated here only when the
+    caller does not pass them)."""
+    _bits16(x, "x"); _u32(qweight, "qweight"); _bits16(scales, "scales")
+    M, N, K = _shape(x, qweight, scales, group)
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if out is None else _cuda(out, "out")
+    a = torch.empty((M,), dtype=torch.int32, device=x.device) if argmax is None else _cuda(argmax, "argmax")
+    _check(_lib.w4a16_gemv_argmax_noalloc(_ptr(y), _ptr(a), _ptr(x), _ptr(qweight), _ptr(scales), M, N, K,
+                                          group, _stream(stream)), "w4a16_gemv_argmax_noalloc")
     return y, a
 
 

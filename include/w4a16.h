@@ -108,6 +108,25 @@ int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32
                       const uint16_t *scales, int M, int N, int K, int group, void *stream);
 
 /*
+ * w4a16_gemv_argmax for callers that cannot allocate device memory (inside a
+ * CUDA graph under a no-new-allocation policy, a plug-in whose host owns every
+ * device allocation, a real-time decode loop that must not reach the driver's
+ * allocator). The pages have no counterpart; this is a library convenience.
+ * Same arguments, layouts, results and errors as w4a16_gemv_argmax, and it runs
+ * the register-streaming decode kernels. It calls no cudaMalloc/cudaFree: its
+ * scratch is a fixed 256 KiB array in the library's device image (held by every
+ * GPU that loads the library until exit), with room for M * CTAs <= 32768 keys;
+ * a larger call (about M * N / 128 > 32768) returns W4_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address for that
+ * device; make that first call before capturing this entry point in a stream.
+ * All calls share the array: calls that overlap in time on the GPU (for
+ * example on two streams) race on it and must be serialized by the caller.
+ */
+int w4a16_gemv_argmax_noalloc(float *y, int32_t *argmax, const uint16_t *x,
+                              const uint32_t *qweight, const uint16_t *scales, int M, int N, int K,
+                              int group, void *stream);
+
+/*
  * 4-bit row gather (the per-layer embedding lookup on the card, Step 2).
  *   out    bf16 [M][K] out: out[t][k] = bf16_rne((code(ids[t], k) - 8) * scale)
  *   ids    int32 [M] device, row indices into the table
