@@ -205,7 +205,7 @@ int w4a16_gemm(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
-    cudaError_t e = w4::run_prefill(y, x, qweight, scales, M, N, K, st->num_sms,
+    cudaError_t e = w4::run_prefill(y, x, qweight, scales, M, N, K, st->num_sms, st->err,
                                     static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported)
         return W4_ERR_UNSUPPORTED;

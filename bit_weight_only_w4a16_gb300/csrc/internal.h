@@ -54,6 +54,6 @@ cudaError_t run_read_probe(unsigned long long *sum, const void *buf, size_t byte
 
 // Prefill (M > 8) tensor-core GEMM.
 cudaError_t run_prefill(float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int M,
-                        int N, int K, int num_sms, cudaStream_t s);
+                        int N, int K, int num_sms, int *err, cudaStream_t s);
 
 } // namespace w4
