@@ -41,6 +41,15 @@ __device__ __forceinline__ uint32_t ldg_nc_u16(const void *p)
     return (uint32_t)v;
 }
 
+// Ask L2 to fetch [p, p + bytes) from HBM without bringing it into the SM.
+// p and bytes must be multiples of 16. L2 is the device's point of coherence,
+// so warming it ahead of griddepcontrol.wait can never make a later load read
+// stale data: a write by the previous kernel still lands in (and updates) L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------- programmatic launch ----
 
 // Let the next kernel on the stream start launching (its own wait still

@@ -25,15 +25,46 @@
 // Kernel "m8" (M = 3..8): lane (g, t) loads word t of one group for rows g and
 // g+8 (32-bit loads); B columns are the x rows; one group per two mmas.
 //
-// Both kernels issue their first weight loads before griddepcontrol.wait, so
-// under programmatic dependent launch the weight stream of this call overlaps
-// the tail of the previous kernel; x is read only after the wait.
+// Both kernels issue their first weight loads (and an L2 prefetch of x) before
+// griddepcontrol.wait, so under programmatic dependent launch the weight
+// stream of this call overlaps the tail of the previous kernel; x is read into
+// the SM only after the wait. Measured on GB300 inside a graph-replayed decode
+// sweep, the time after the wait is latency, not bandwidth: the x round trip
+// and the per-warp chain of dependent mmas. Hence small shapes split K finely
+// (one to three k-tiles per warp, up to 16 warps per row block), x is staged
+// with all of a thread's loads in flight at once, and the 8 mmas of a k-tile
+// accumulate into two independent chains.
 #include "common.cuh"
 #include "internal.h"
 
 namespace w4 {
 
 static constexpr int kTileK = 128; // k per tile of the m2 kernel: 4 groups
+
+// xs[m * cpr + c] = permute_x8(x[m][8c .. 8c+7]) for m < rows, c < cpr (chunks
+// at or past K/8 are zero). Each thread issues up to kXLoads loads before it
+// uses any, so the staging costs one memory round trip, not one per chunk.
+__device__ __forceinline__ void stage_x_rows(uint4 *xs, const uint16_t *x, int rows, int K, int cpr)
+{
+    constexpr int kXLoads = 4;
+    const int total = rows * cpr, kc = K >> 3;
+    for (int i0 = threadIdx.x; i0 < total; i0 += kXLoads * blockDim.x) {
+        uint4 v[kXLoads];
+#pragma unroll
+        for (int j = 0; j < kXLoads; ++j) {
+            const int i = i0 + j * blockDim.x;
+            const int m = i / cpr, c = i - m * cpr;
+            v[j] = (i < total && c < kc) ? *reinterpret_cast<const uint4 *>(x + (size_t)m * K + c * 8)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kXLoads; ++j) {
+            const int i = i0 + j * blockDim.x;
+            if (i < total)
+                xs[i] = permute_x8(v[j]);
+        }
+    }
+}
 
 // ---------------------------------------------------------------- m2 ----
 
@@ -90,6 +121,8 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     };
 
     // Stream the first weight tiles before waiting on the previous kernel.
+    if (threadIdx.x == 32)
+        prefetch_l2_bulk(x, (uint32_t)(MX * K * 2));
 #pragma unroll
     for (int u = 0; u < U; ++u)
         if (u < nkt)
@@ -100,13 +133,7 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     // Stage x, permuted into the B-operand pair order, and a zero chunk.
     uint4 *xs = reinterpret_cast<uint4 *>(smem);
     const int chunks_per_row = Kpad >> 3;
-    for (int i = threadIdx.x; i < MX * chunks_per_row; i += blockDim.x) {
-        const int m = i / chunks_per_row, c = i - m * chunks_per_row;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (c * 8 < K)
-            v = permute_x8(*reinterpret_cast<const uint4 *>(x + (size_t)m * K + c * 8));
-        xs[i] = v;
-    }
+    stage_x_rows(xs, x, MX, K, chunks_per_row);
     uint4 *zero_chunk = xs + MX * chunks_per_row;
     if (threadIdx.x == 0)
         *zero_chunk = make_uint4(0u, 0u, 0u, 0u);
@@ -123,7 +150,8 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     float accA = 0.f, accB = 0.f;
 
     auto compute = [&](int u, int kt) {
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        // Two independent accumulator chains (4 mmas each) instead of one of 8.
+        float c[4] = {0.f, 0.f, 0.f, 0.f}, d[4] = {0.f, 0.f, 0.f, 0.f};
         const uint4 *xb = xrow + xstep * kt;
         const uint32_t a_w[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
         const uint32_t b_w[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
@@ -134,12 +162,12 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
             unpack_word(a_w[i], a04, a15, a26, a37);
             unpack_word(b_w[i], b04, b15, b26, b37);
             mma_16816(c, a04, b04, a15, b15, b.x, b.y);
-            mma_16816(c, a26, b26, a37, b37, b.z, b.w);
+            mma_16816(d, a26, b26, a37, b37, b.z, b.w);
         }
-        accA = fmaf(bf16lo_to_f32(sa[u]), c[0], accA);
-        accA = fmaf(bf16hi_to_f32(sa[u]), c[1], accA);
-        accB = fmaf(bf16lo_to_f32(sb[u]), c[2], accB);
-        accB = fmaf(bf16hi_to_f32(sb[u]), c[3], accB);
+        accA = fmaf(bf16lo_to_f32(sa[u]), c[0] + d[0], accA);
+        accA = fmaf(bf16hi_to_f32(sa[u]), c[1] + d[1], accA);
+        accB = fmaf(bf16lo_to_f32(sb[u]), c[2] + d[2], accB);
+        accB = fmaf(bf16hi_to_f32(sb[u]), c[3] + d[3], accB);
     };
 
     for (int base = 0; base < nkt; base += U) {
@@ -250,6 +278,8 @@ gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         }
     };
 
+    if (threadIdx.x == 32)
+        prefetch_l2_bulk(x, (uint32_t)(M * K * 2));
 #pragma unroll
     for (int u = 0; u < U; ++u)
         if (u < nG)
@@ -259,13 +289,10 @@ gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 
     uint4 *xs = reinterpret_cast<uint4 *>(smem); // [8][K/8] permuted chunks
     const int cpr = K >> 3;
-    for (int i = threadIdx.x; i < 8 * cpr; i += blockDim.x) {
-        const int m = i / cpr, c = i - m * cpr;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (m < M)
-            v = permute_x8(*reinterpret_cast<const uint4 *>(x + (size_t)m * K + c * 8));
-        xs[i] = v;
-    }
+    stage_x_rows(xs, x, M, K, cpr);
+    if (M < 8) // rows M..7 of the B operand are zero
+        for (int i = M * cpr + threadIdx.x; i < 8 * cpr; i += blockDim.x)
+            xs[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
     // B column g is x-row g; this lane supplies word t of each group.
@@ -410,15 +437,35 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
     DecodePlan p;
     const int nrb = (N + 15) / 16;
     if (M <= 2) {
+        // Split K until ~12 warps per SM carry the stream, down to one k-tile
+        // per warp, as long as the whole grid is resident at once (a second
+        // wave of CTAs costs a full memory round trip). Rows that leave more
+        // than 4 k-tiles per warp keep 8 of them in flight (128 registers a
+        // thread instead of <= 96).
         const int T = (K + kTileK - 1) / kTileK;
-        const int target = num_sms * 12; // warps in flight for the weight stream
-        int ks = 1;
-        while (ks < 16 && (long long)nrb * ks < target && T >= 4 * ks)
-            ks *= 2;
-        p.kernel = 2;
-        p.ksplit = ks;
-        p.warps = ks >= 8 ? ks : 8;
-        p.unroll = 4;
+        const int target = num_sms * 12;
+        auto make = [&](int ks) {
+            DecodePlan q;
+            q.kernel = 2;
+            q.ksplit = ks;
+            q.warps = ks >= 8 ? ks : 8;
+            q.unroll = (T + ks - 1) / ks > 4 ? 8 : 4;
+            q.grid = (nrb + q.warps / ks - 1) / (q.warps / ks);
+            return q;
+        };
+        auto resident = [&](const DecodePlan &q) {
+            const int regs = q.unroll == 8 ? 128 : 96;
+            const int per_sm = (65536 / (regs * 32)) / q.warps;
+            return (long long)q.grid <= (long long)num_sms * per_sm;
+        };
+        p = make(1);
+        for (int ks = 2; ks <= 16 && ks <= T && (long long)nrb * p.ksplit < target; ks *= 2) {
+            const DecodePlan q = make(ks);
+            if (!resident(q))
+                break;
+            p = q;
+        }
+        return p;
     } else {
         const int ngroups = K / 32;
         const int target = num_sms * 12;
@@ -447,6 +494,8 @@ static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, c
         smem += (size_t)rbc * p.ksplit * MX * 16 * sizeof(float);
     const bool sc32 = (K % 64) == 0;
     auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, ARGMAX> : gemv_m2_kernel<MX, 4, false, ARGMAX>;
+    if (p.unroll == 8)
+        kern = sc32 ? gemv_m2_kernel<MX, 8, true, ARGMAX> : gemv_m2_kernel<MX, 8, false, ARGMAX>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;

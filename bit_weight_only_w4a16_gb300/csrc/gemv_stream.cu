@@ -540,13 +540,15 @@ bool stream_supported(int M, int N, int K, const void *qw, const void *sc)
 bool stream_preferred(int M, int N, int K)
 {
     // Measured on GB300 in a 20-launch CUDA graph per shape (programmatic
-    // dependent launch): the tensor-copy kernel wins on the wide K = 1536
-    // shapes (gate|up 12288 and 24576 rows: 5.8 vs 5.9 us, 10.2 vs 10.8 us) and
-    // loses on the small and long-K ones (q|k|v 3.3 vs 2.4 us, o 3.5 vs 2.3 us,
-    // down 6.5 vs 3.7 us and 10.3 vs 6.4 us), where its fixed per-kernel cost
-    // and its K-split clusters do not pay off.
+    // dependent launch), after the register kernel's K-split and preload were
+    // tuned for single-wave residency: the register kernel wins on every decode
+    // shape of the sweep (q|k|v 2.5 vs 3.3 us, o 2.4 vs 3.5, gate|up 12288
+    // 4.7 vs 5.8, down 6144 3.7 vs 6.4, gate|up 24576 7.5 vs 10.2, down 12288
+    // 5.5 vs 10.3), so the tensor-copy kernel is chosen only on request.
     (void)M;
-    return (long long)N * K >= (long long)12288 * 1536 && K <= 1536;
+    (void)N;
+    (void)K;
+    return false;
 }
 
 StreamPlan plan_stream(int M, int N, int K, int num_sms)
