@@ -174,30 +174,44 @@ class ClockSampler:
 
 # ----------------------------------------------------------- reference ----
 
-def oracle_sample(budget_s: float = 12.0):
-    """Time the fp64 CPU oracle over whole sweep stages until ~budget_s of work.
+_ORACLE_INPUTS = {}
 
-    Returns (GB/s of algorithmic sweep bytes, description of the sample, seconds).
-    """
-    import oracle
-    done_bytes, t_total, stages = 0, 0.0, 0
-    order = [(l, s) for l in (0, 15, 1, 16, 2, 17, 3, 18) for s in fused_stages(l)]
-    for l, (name, members, N, K) in order:
+
+def _stage_inputs(l, members, K):
+    """Host copies of one fused stage's x, codes and steps (cached across calls)."""
+    key = (l, tuple(members))
+    if key not in _ORACLE_INPUTS:
         x = synth.gen_x(seed_of(l, members[0]), 1, K)
         qws, scs = [], []
         for p in members:
             n_p = next(n for nm, n, _ in layer_shapes(l) if nm == p)
             qws.append(synth.gen_qweight(seed_of(l, p), n_p, K))
             scs.append(synth.gen_scales(seed_of(l, p), n_p, K))
-        qw, sc = np.concatenate(qws), np.concatenate(scs)
+        _ORACLE_INPUTS[key] = (x, np.concatenate(qws), np.concatenate(scs))
+    return _ORACLE_INPUTS[key]
+
+
+def oracle_sample(budget_s: float = 12.0, max_stages: int = 16 * LAYERS):
+    """Time the fp64 CPU oracle over sweep stages, in sweep order, until ~budget_s of work.
+
+    Stages are taken in the sweep's own order (layer 0 q|k|v, o, gate|up, down,
+    layer 1, ...), at most max_stages of them, wrapping around the sweep if the
+    budget is not used up. Returns (GB/s of algorithmic sweep bytes, description
+    of the sample, seconds of oracle time).
+    """
+    import oracle
+    order = [(l, st) for l in range(LAYERS) for st in fused_stages(l)]
+    done_bytes, t_total, stages = 0, 0.0, 0
+    while t_total < budget_s and stages < max_stages:
+        l, (name, members, N, K) = order[stages % len(order)]
+        x, qw, sc = _stage_inputs(l, members, K)
         t0 = time.perf_counter()
         oracle.gemm(x, qw, sc)
         t_total += time.perf_counter() - t0
         done_bytes += stage_bytes(N, K)
         stages += 1
-        if t_total >= budget_s:
-            break
-    desc = f"{stages} fused stages of layers 0,15,1,16,... ({done_bytes / 1e6:.1f} MB of the sweep)"
+    desc = (f"{stages} fused stages taken in sweep order, wrapping after all {len(order)} "
+            f"({stages / len(order):.2f} sweeps, {done_bytes / 1e6:.1f} MB)")
     return done_bytes / t_total / 1e9, desc, t_total
 
 
@@ -231,6 +245,24 @@ def measured_peaks():
         return float(p["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback"
+
+
+def captured_traffic():
+    """DRAM bytes (read + write) of one sweep from the committed ncu capture, or
+    None when the decode kernel's sources changed after that capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemv_m2_decode_sweep_traffic.json")) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def run_ours(args, rank, world):
@@ -372,7 +404,9 @@ def run_ours(args, rank, world):
                    "l2": "inputs larger than L2 (1.02 GB per sweep vs 129 MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": captured_traffic(),
+                     "traffic_unit": "bytes per sweep (140 launches), ncu dram__bytes_read.sum + "
+                                     "dram__bytes_write.sum; null if the kernel changed since",
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "kernel": "gemv_m2_kernel (all 140 launches of the sweep)"},
         "probe": {"hbm_read_probe_gbs": probe_gbs, "sweep_frac_of_probe": achieved / probe_gbs},
@@ -385,15 +419,60 @@ def run_ours(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
+def run_ncu_case(case: str):
+    """One small fixed case for an ncu capture: no timing, no output but "ok".
+
+    decode_shapes : w4a16_gemv, M=1, twice on each of (24576,1536) (1536,12288)
+                    (2560,1536), writing a 256 MB buffer between calls.
+    prefill:NxK   : w4a16_gemm twice with M=1024 tokens on an N x K weight.
+    """
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_weight_only_w4a16_gb300 as w4
+    torch.cuda.set_device(0)
+    w4.init()
+    dev = torch.device("cuda", 0)
+
+    def problem(seed, M, N, K):
+        x = torch.from_numpy(synth.gen_x(seed + 2, M, K).view(np.int16)).to(dev)
+        q = synth.gen_qweight_torch(seed, N, K, dev)
+        sc = torch.from_numpy(synth.gen_scales(seed, N, K).view(np.int16)).to(dev)
+        return x, q, sc
+
+    if case == "decode_shapes":
+        data = [problem(100 + i, 1, N, K) for i, (N, K) in enumerate([(24576, 1536), (1536, 12288), (2560, 1536)])]
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for rep in range(2):
+            for x, q, sc in data:
+                flush.fill_(rep)
+                w4.w4a16_gemv(x, q, sc)
+    elif case.startswith("prefill:"):
+        N, K = (int(v) for v in case.split(":")[1].split("x"))
+        x, q, sc = problem(3000, 1024, N, K)
+        for _ in range(2):
+            w4.w4a16_gemm(x, q, sc)
+    else:
+        raise SystemExit(f"unknown --ncu-case {case}")
+    torch.cuda.synchronize()
+    print("ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", default=None,
+                    help="run one small fixed case for an ncu capture instead of the bench: "
+                         "decode_shapes | prefill:NxK")
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case(args.ncu_case)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
