@@ -68,7 +68,10 @@ __device__ __forceinline__ void stage_x_rows(uint4 *xs, const uint16_t *x, int r
 
 // ---------------------------------------------------------------- m2 ----
 
-template <int MX, int U, bool SC32, bool ARGMAX>
+// FULL (K % 128 == 0, implies SC32): every k-tile is whole, so the loads need
+// no per-group guards; warps past the last row block load clamped rows and
+// never store.
+template <int MX, int U, bool SC32, bool FULL, bool ARGMAX>
 __global__ void __launch_bounds__(512)
 gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
@@ -100,6 +103,13 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     uint32_t sa[U], sb[U];
 
     auto load = [&](int u, int kt) {
+        if (FULL) {
+            wa[u] = ldg_stream_v4(qA + 16 * kt);
+            wb[u] = ldg_stream_v4(qB + 16 * kt);
+            sa[u] = ldg_nc_u32(sA + 4 * kt);
+            sb[u] = ldg_nc_u32(sB + 4 * kt);
+            return;
+        }
         const int G = 4 * kt + t;
         if (active && G < ngroups) {
             wa[u] = ldg_stream_v4(qA + 16 * kt);
@@ -492,10 +502,12 @@ static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, c
     size_t smem = (size_t)MX * Kpad * 2 + 16;
     if (p.ksplit > 1)
         smem += (size_t)rbc * p.ksplit * MX * 16 * sizeof(float);
-    const bool sc32 = (K % 64) == 0;
-    auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, ARGMAX> : gemv_m2_kernel<MX, 4, false, ARGMAX>;
+    const bool sc32 = (K % 64) == 0, full = (K % kTileK) == 0;
+    auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, false, ARGMAX> : gemv_m2_kernel<MX, 4, false, false, ARGMAX>;
     if (p.unroll == 8)
-        kern = sc32 ? gemv_m2_kernel<MX, 8, true, ARGMAX> : gemv_m2_kernel<MX, 8, false, ARGMAX>;
+        kern = sc32 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX> : gemv_m2_kernel<MX, 8, false, false, ARGMAX>;
+    if (full)
+        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX> : gemv_m2_kernel<MX, 4, true, true, ARGMAX>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
