@@ -14,12 +14,15 @@ namespace {
 constexpr int kMaxDevices = 64;
 // Argmax scratch: one 64-bit key per (x-row, CTA); 8 rows x 65536 CTAs.
 constexpr size_t kKeyCapacity = 8u * 65536u;
+// Prefill split-K scratch: 8 Mi fp32 partials (32 MiB).
+constexpr size_t kWsFloats = 8u << 20;
 
 struct DeviceState {
     bool ready = false;
     int num_sms = 0;
     unsigned long long *keys = nullptr;
     int *err = nullptr; // device error word written by kernels whose bounded waits ran out
+    float *ws = nullptr; // prefill split-K partials
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -86,6 +89,11 @@ int device_state(DeviceState **out)
         e = cudaMemset(st.err, 0, sizeof(int));
         if (e != cudaSuccess)
             return cuda_fail(e);
+        void *w = nullptr;
+        e = cudaMalloc(&w, kWsFloats * sizeof(float));
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+        st.ws = static_cast<float *>(w);
         st.num_sms = sms;
         st.ready = true;
     }
@@ -205,7 +213,8 @@ int w4a16_gemm(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
-    cudaError_t e = w4::run_prefill(y, x, qweight, scales, M, N, K, st->num_sms, st->err,
+    const w4::PrefillPlan p = w4::plan_prefill(M, N, K, st->num_sms, kWsFloats);
+    cudaError_t e = w4::run_prefill(p, y, x, qweight, scales, M, N, K, st->ws, st->err,
                                     static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported)
         return W4_ERR_UNSUPPORTED;

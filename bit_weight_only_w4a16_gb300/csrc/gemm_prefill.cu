@@ -12,15 +12,24 @@
 // accumulate. Rounding each weight to bf16 (relative error <= 2^-9) keeps the
 // result within 2e-3 * sum|w x|.
 //
-// Tile: 128 weight rows (the MMA's M, TMEM lanes) x 256 tokens (the MMA's N,
-// TMEM columns) x 64 k per stage (one 128-byte swizzle row of bf16), 4 stages.
-//   warp 0    : TMA of the x tile (256 tokens x 64 k, 128-byte swizzle), the B operand
-//   warp 1    : allocates 256 TMEM columns; lane 0 issues tcgen05.mma (4 x K=16 per
-//               stage) and commits each stage's slot back to the producers
-//   warps 2-5 : one thread per weight row: load 8 code words + 2 steps, dequantize
-//               to bf16 and store the A tile in the K-major 128-byte-swizzle layout
-//               the MMA reads; then the epilogue: tcgen05.ld of their 32 TMEM
-//               lanes and coalesced fp32 stores of y.
+// Persistent kernel, one CTA per SM. A work item is a tile of 128 weight rows
+// (the MMA's M, TMEM lanes) x 256 tokens (the MMA's N) over a range of K. Whole
+// tiles are dealt round-robin to the CTAs for as many full rounds as there are;
+// the remaining tiles are split along K into S parts so that the last round
+// spreads over all SMs (S = 1 when the tiles divide evenly). Every role walks
+// the same item sequence.
+//   warp 0     : TMA of the x tiles (256 tokens x 64 k, 128-byte swizzle) - B operand
+//   warp 1     : allocates 512 TMEM columns (two accumulators); lane 0 issues
+//                tcgen05.mma (4 x K=16 per stage) and commits each stage's slot
+//                back to the producers and each finished accumulator to the epilogue
+//   warps 2-9  : two threads per weight row (32 k each): codes and step six
+//                stages ahead in registers, dequantized to bf16 into the K-major
+//                128-byte-swizzle A tile the MMA reads
+//   warps 10-13: epilogue: tcgen05.ld of their 32 TMEM lanes, coalesced fp32
+//                stores of y, or for a split tile of its partial.
+// A second kernel adds the S partials of each split tile in split order (a
+// fixed order: the result does not depend on timing) and writes y.
+// The epilogue of item j overlaps the MMAs of item j+1 (double-buffered TMEM).
 // Every wait is bounded; a timeout sets the device error word and the kernel
 // still drains its copies and MMAs and frees TMEM before returning.
 #include "common.cuh"
@@ -35,17 +44,21 @@ namespace w4 {
 
 namespace {
 
-constexpr int kBM = 128;  // weight rows per tile
-constexpr int kBN = 256;  // tokens per tile
-constexpr int kBK = 64;   // k per stage
+constexpr int kBM = 128; // weight rows per tile
+constexpr int kBN = 256; // tokens per tile
+constexpr int kBK = 64;  // k per stage
 constexpr int kStages = 4;
+constexpr int kDqWarps = 8;
+constexpr int kDqAhead = 6; // k-stages of codes in flight per dequant thread
+constexpr int kEpiWarp0 = 2 + kDqWarps; // first epilogue warp
+constexpr int kThreads = (kEpiWarp0 + 4) * 32;
 constexpr int kASlot = kBM * kBK * 2; // 16 KiB
 constexpr int kBSlot = kBN * kBK * 2; // 32 KiB
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr size_t kSmem = (size_t)kStages * (kASlot + kBSlot) + 1024;
+constexpr int kTileFloats = kBM * kBN;
 constexpr int kWait = 1 << 16;
 constexpr int kDrain = 64;
-constexpr size_t kSmem = (size_t)kStages * (kASlot + kBSlot) + 1024;
 
 // tcgen05 instruction descriptor, kind::f16: fp32 D, bf16 A and B, both
 // K-major, N = kBN, M = kBM.
@@ -57,10 +70,10 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN
 __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr)
 {
     uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;            // leading byte offset (unused for this layout): 16 B
-    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 B
-    d |= (uint64_t)1 << 46;            // descriptor version
-    d |= (uint64_t)2 << 61;            // 128-byte swizzle
+    d |= (uint64_t)1 << 16;           // leading byte offset (unused for this layout): 16 B
+    d |= (uint64_t)(1024 >> 4) << 32; // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;           // descriptor version
+    d |= (uint64_t)2 << 61;           // 128-byte swizzle
     return d;
 }
 
@@ -99,8 +112,8 @@ __device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint3
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t step2, uint32_t &p01, uint32_t &p23,
                                              uint32_t &p45, uint32_t &p67)
 {
-    const uint32_t lo = w & 0x0F0F0F0Fu;         // codes k0 k2 k4 k6 in bytes 0..3
-    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;  // codes k1 k3 k5 k7
+    const uint32_t lo = w & 0x0F0F0F0Fu;             // codes k0 k2 k4 k6 in bytes 0..3
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;      // codes k1 k3 k5 k7
     const uint32_t m0 = __byte_perm(lo, hi, 0x5140); // k0 k1 k2 k3
     const uint32_t m1 = __byte_perm(lo, hi, 0x7362); // k4 k5 k6 k7
     // 0x43 high bytes: bf16 of 128 + code
@@ -121,16 +134,44 @@ struct PrefillArgs {
     float *y;
     const uint32_t *qw;
     const uint16_t *sc;
+    float *ws; // split partials, one kTileFloats slot per (split tile, split)
     int *err;
     int M, N, K;
+    int tiles_n;  // 128-row weight tiles
+    int tiles;    // tiles_n * 256-token tiles
+    int full;     // tiles computed whole (the first full rounds)
+    int S;        // K splits of each of the remaining tiles
+    int items;    // full + (tiles - full) * S
 };
+
+// Item i -> tile t (weight tile t % tiles_n, token tile t / tiles_n), its split
+// s of S (S = 1 for whole tiles). Consecutive items share the token tile, so
+// CTAs working at the same time read the same x rows.
+struct Item {
+    int t, s, S;
+};
+__device__ __forceinline__ Item item_of(const PrefillArgs &a, int i)
+{
+    Item it;
+    if (i < a.full) {
+        it.t = i;
+        it.s = 0;
+        it.S = 1;
+    } else {
+        const int j = i - a.full, rem = a.tiles - a.full;
+        it.t = a.full + j % rem;
+        it.s = j / rem;
+        it.S = a.S;
+    }
+    return it;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap xmap)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) unsigned long long full_a[kStages], full_b[kStages], empty[kStages];
-    __shared__ __align__(8) unsigned long long acc_full;
+    __shared__ __align__(8) unsigned long long acc_full[2], acc_empty[2];
     __shared__ uint32_t tmem_base;
     __shared__ int s_abort;
 
@@ -139,17 +180,18 @@ gemm_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap xma
     const uint32_t b_ring = a_ring + kStages * kASlot;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * kBM;  // first weight row of the tile
-    const int m0 = blockIdx.y * kBN;  // first token of the tile
-    const int nst = a.K / kBK;
+    const int nst = a.K / kBK; // k-stages of a whole row
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_addr(&full_a[s]), kBM);
+            mbar_init(smem_addr(&full_a[s]), kDqWarps); // one arrival per dequant warp
             mbar_init(smem_addr(&full_b[s]), 1);
             mbar_init(smem_addr(&empty[s]), 1);
         }
-        mbar_init(smem_addr(&acc_full), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_addr(&acc_full[b]), 1);
+            mbar_init(smem_addr(&acc_empty[b]), 4); // one arrival per epilogue warp
+        }
         s_abort = 0;
         fence_mbar_init();
     }
@@ -168,110 +210,170 @@ gemm_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap xma
         s_abort = 1;
         atomicOr(a.err, 2);
     };
+    auto wait = [&](unsigned long long &bar, uint32_t parity) {
+        if (!mbar_wait_bounded(smem_addr(&bar), parity, s_abort ? kDrain : kWait))
+            fail();
+    };
+    auto k_begin = [&](const Item &it, int s) { return (int)((long long)nst * s / it.S); };
 
     if (warp == 0) {
         // ------------------------------------------------ x tiles (TMA)
         if (lane == 0) {
-            for (int i = 0; i < nst; ++i) {
-                const int s = i % kStages, u = i / kStages;
-                if (u > 0 && !mbar_wait_bounded(smem_addr(&empty[s]), (u - 1) & 1, s_abort ? kDrain : kWait))
-                    fail();
-                const uint32_t bar = smem_addr(&full_b[s]);
-                mbar_arrive_expect_tx(bar, kBSlot);
-                tma_load_2d(b_ring + s * kBSlot, &xmap, i * kBK, m0, bar);
+            uint32_t g = 0;
+            for (int i = blockIdx.x; i < a.items; i += gridDim.x) {
+                const Item it = item_of(a, i);
+                const int k0 = k_begin(it, it.s), k1 = k_begin(it, it.s + 1);
+                const int m0 = (it.t / a.tiles_n) * kBN;
+                for (int st = k0; st < k1; ++st, ++g) {
+                    const uint32_t slot = g % kStages, u = g / kStages;
+                    if (u > 0)
+                        wait(empty[slot], (u - 1) & 1);
+                    const uint32_t bar = smem_addr(&full_b[slot]);
+                    mbar_arrive_expect_tx(bar, kBSlot);
+                    tma_load_2d(b_ring + slot * kBSlot, &xmap, st * kBK, m0, bar);
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue
         if (lane == 0) {
-            for (int i = 0; i < nst; ++i) {
-                const int s = i % kStages, u = i / kStages;
-                if (!mbar_wait_bounded(smem_addr(&full_b[s]), u & 1, s_abort ? kDrain : kWait))
-                    fail();
-                if (!mbar_wait_bounded(smem_addr(&full_a[s]), u & 1, s_abort ? kDrain : kWait))
-                    fail();
+            uint32_t g = 0, j = 0;
+            for (int i = blockIdx.x; i < a.items; i += gridDim.x, ++j) {
+                const Item it = item_of(a, i);
+                const int k0 = k_begin(it, it.s), k1 = k_begin(it, it.s + 1);
+                const uint32_t b = j & 1, uj = j >> 1;
+                if (j >= 2)
+                    wait(acc_empty[b], (uj - 1) & 1);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint64_t ad = sdesc_k128(a_ring + s * kASlot);
-                const uint64_t bd = sdesc_k128(b_ring + s * kBSlot);
+                const uint32_t acc = tmem + b * kBN;
+                for (int st = k0; st < k1; ++st, ++g) {
+                    const uint32_t slot = g % kStages, u = g / kStages;
+                    wait(full_b[slot], u & 1);
+                    wait(full_a[slot], u & 1);
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint64_t ad = sdesc_k128(a_ring + slot * kASlot);
+                    const uint64_t bd = sdesc_k128(b_ring + slot * kBSlot);
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k) // +32 bytes of K per step
-                    mma_bf16(tmem, ad + 2u * k, bd + 2u * k, kIdesc, (i | k) != 0);
-                mma_commit(smem_addr(&empty[s]));
+                    for (int k = 0; k < kBK / 16; ++k) // +32 bytes of K per step
+                        mma_bf16(acc, ad + 2u * k, bd + 2u * k, kIdesc, (st > k0 || k > 0) ? 1u : 0u);
+                    mma_commit(smem_addr(&empty[slot]));
+                }
+                mma_commit(smem_addr(&acc_full[b]));
             }
-            mma_commit(smem_addr(&acc_full));
         }
-    } else {
+    } else if (warp < kEpiWarp0) {
         // ------------------------------------------------ A tiles (dequant)
-        const int r = threadIdx.x - 64; // row of the tile, 0..127
-        const int n = n0 + r;
-        const bool valid = n < a.N;
-        const uint32_t *qrow = a.qw + (size_t)(valid ? n : 0) * (a.K >> 3);
-        const uint16_t *srow = a.sc + (size_t)(valid ? n : 0) * (a.K >> 5);
+        const int d = threadIdx.x - 64;
+        const int r = d & (kBM - 1); // row of the tile
+        const int h = d >> 7;        // which 32 k of the stage: group 2st + h
         const uint32_t rowoff = (uint32_t)r * 128u;
         const uint32_t sw = (uint32_t)(r & 7);
-        uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
-        uint32_t s01 = 0u;
-        auto load = [&](int i) {
-            if (valid) {
-                w0 = ldg_stream_v4(qrow + 8 * i);
-                w1 = ldg_stream_v4(qrow + 8 * i + 4);
-                s01 = ldg_nc_u32(srow + 2 * i);
-            }
-        };
-        load(0);
-        for (int i = 0; i < nst; ++i) {
-            const int s = i % kStages, u = i / kStages;
-            const uint4 c0 = w0, c1 = w1;
-            const uint32_t st = s01;
-            if (i + 1 < nst)
-                load(i + 1); // next stage's codes in flight while this one is stored
-            if (u > 0 && !mbar_wait_bounded(smem_addr(&empty[s]), (u - 1) & 1, s_abort ? kDrain : kWait))
-                fail();
-            const uint32_t base = a_ring + s * kASlot + rowoff;
-            const uint32_t sa = valid ? __byte_perm(st, st, 0x1010) : 0u; // group 2i, both halves
-            const uint32_t sb = valid ? __byte_perm(st, st, 0x3232) : 0u; // group 2i + 1
-            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t g = 0;
+        for (int i = blockIdx.x; i < a.items; i += gridDim.x) {
+            const Item it = item_of(a, i);
+            const int k0 = k_begin(it, it.s), k1 = k_begin(it, it.s + 1);
+            const int n = (it.t % a.tiles_n) * kBM + r;
+            const bool valid = n < a.N;
+            const uint32_t *qrow = a.qw + (size_t)(valid ? n : 0) * (a.K >> 3) + 4 * h;
+            const uint16_t *srow = a.sc + (size_t)(valid ? n : 0) * (a.K >> 5) + h;
+            // Codes and step of the next kDqAhead stages in flight: stage st lives
+            // in register set (st - k0) % kDqAhead, refilled with st + kDqAhead as
+            // soon as it is consumed (no register copies, which would wait for the
+            // load in flight).
+            uint4 cw[kDqAhead];
+            uint32_t cs[kDqAhead];
+            auto load = [&](int st, uint4 &w, uint32_t &s1) {
+                if (valid && st < k1) {
+                    w = ldg_stream_v4(qrow + 8 * st);
+                    s1 = ldg_nc_u16(srow + 2 * st);
+                } else {
+                    w = make_uint4(0u, 0u, 0u, 0u);
+                    s1 = 0u;
+                }
+            };
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint32_t p01, p23, p45, p67;
-                dequant_word(words[j], j < 4 ? sa : sb, p01, p23, p45, p67);
-                if (!valid)
-                    p01 = p23 = p45 = p67 = 0u;
-                sts128(base + ((((uint32_t)j) ^ sw) << 4), p01, p23, p45, p67);
-            }
-            // Generic-proxy stores must be visible to the tensor core (async proxy).
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(smem_addr(&full_a[s]));
-        }
-
-        // ------------------------------------------------ epilogue
-        if (!mbar_wait_bounded(smem_addr(&acc_full), 0, s_abort ? kDrain : kWait))
-            fail();
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const int q = warp & 3;               // TMEM lane quarter this warp may read
-        const int row = n0 + 32 * q + lane;   // weight row = output column of y
-        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
-            uint32_t v[32];
-            asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-                         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-                         "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-                         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                           "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
-                           "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
-                           "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-                           "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]),
-                           "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-                         : "r"(taddr + (uint32_t)c0));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            if (row < a.N) {
+            for (int u = 0; u < kDqAhead; ++u)
+                load(k0 + u, cw[u], cs[u]);
+            for (int base = k0; base < k1; base += kDqAhead) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int m = m0 + c0 + j;
-                    if (m < a.M)
-                        a.y[(size_t)m * a.N + row] = __uint_as_float(v[j]);
+                for (int u = 0; u < kDqAhead; ++u) {
+                    const int st = base + u;
+                    if (st < k1) {
+                        const uint32_t slot = g % kStages, uu = g / kStages;
+                        if (uu > 0)
+                            wait(empty[slot], (uu - 1) & 1);
+                        const uint32_t dst = a_ring + slot * kASlot + rowoff;
+                        const uint32_t step2 = valid ? (cs[u] | (cs[u] << 16)) : 0u;
+                        const uint32_t words[4] = {cw[u].x, cw[u].y, cw[u].z, cw[u].w};
+#pragma unroll
+                        for (int jw = 0; jw < 4; ++jw) {
+                            uint32_t p01, p23, p45, p67;
+                            dequant_word(words[jw], step2, p01, p23, p45, p67);
+                            if (!valid)
+                                p01 = p23 = p45 = p67 = 0u;
+                            sts128(dst + ((((uint32_t)(4 * h + jw)) ^ sw) << 4), p01, p23, p45, p67);
+                        }
+                        // Generic-proxy stores must be visible to the tensor core
+                        // (async proxy); then one arrival for the warp.
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(smem_addr(&full_a[slot]));
+                        load(st + kDqAhead, cw[u], cs[u]);
+                        ++g;
+                    }
                 }
             }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int q = warp & 3; // TMEM lane quarter this warp may read
+        const int e = threadIdx.x - kEpiWarp0 * 32;
+        uint32_t j = 0;
+        for (int i = blockIdx.x; i < a.items; i += gridDim.x, ++j) {
+            const Item it = item_of(a, i);
+            const uint32_t b = j & 1, uj = j >> 1;
+            const int n0 = (it.t % a.tiles_n) * kBM, m0 = (it.t / a.tiles_n) * kBN;
+            const bool split = it.S > 1;
+            wait(acc_full[b], uj & 1);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const int rl = 32 * q + lane; // row of the tile
+            const int row = n0 + rl;      // weight row = output column of y
+            // A split tile's partial goes to its slot, token-major [256][128].
+            float *part = split ? a.ws + ((size_t)(it.t - a.full) * it.S + it.s) * kTileFloats : nullptr;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + b * kBN;
+            for (int c0 = 0; c0 < kBN; c0 += 32) {
+                uint32_t v[32];
+                asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                             "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                             "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                             : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                               "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                               "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+                               "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                               "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]),
+                               "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                             : "r"(taddr + (uint32_t)c0));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (split) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj)
+                        part[(c0 + jj) * kBM + rl] = __uint_as_float(v[jj]);
+                } else if (row < a.N) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int m = m0 + c0 + jj;
+                        if (m < a.M)
+                            a.y[(size_t)m * a.N + row] = __uint_as_float(v[jj]);
+                    }
+                }
+            }
+            // This accumulator may be overwritten by the MMAs of item j + 2.
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&acc_empty[b]));
+
         }
     }
 
@@ -280,6 +382,49 @@ gemm_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap xma
     if (warp == 1) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// y of the split tiles: the S partials of each, added in split order. One CTA
+// of 256 threads per (split tile, 32-token slice); thread i handles 4 weight
+// rows (float4) of 4 tokens of the slice.
+__global__ void __launch_bounds__(256)
+prefill_split_reduce_kernel(float *__restrict__ y, const float *__restrict__ ws, int M, int N, int tiles_n,
+                            int full, int S)
+{
+    const int st = blockIdx.x; // split tile index
+    const int t = full + st;
+    const int n0 = (t % tiles_n) * kBM, m0 = (t / tiles_n) * kBN;
+    const int r4 = 4 * (threadIdx.x & 31);
+    const int tok0 = blockIdx.y * 32 + (threadIdx.x >> 5) * 4;
+    const float4 *base = reinterpret_cast<const float4 *>(ws + (size_t)st * S * kTileFloats);
+    float4 acc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            v[u] = __ldcs(base + ((size_t)s * kTileFloats + (size_t)(tok0 + u) * kBM + r4) / 4);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            acc[u].x += v[u].x;
+            acc[u].y += v[u].y;
+            acc[u].z += v[u].z;
+            acc[u].w += v[u].w;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int m = m0 + tok0 + u;
+        if (m >= M)
+            continue;
+        const float o[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            if (n0 + r4 + c < N)
+                y[(size_t)m * N + n0 + r4 + c] = o[c];
     }
 }
 
@@ -298,20 +443,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder()
     return fn;
 }
 
-} // namespace
-
-cudaError_t run_prefill(float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int M,
-                        int N, int K, int num_sms, int *err, cudaStream_t s)
+cudaError_t launch(const PrefillArgs &a, const uint16_t *x, int grid, cudaStream_t s)
 {
-    (void)num_sms;
-    if (K % kBK != 0 || N % 16 != 0)
-        return cudaErrorNotSupported;
     auto enc = encoder();
     if (!enc)
         return cudaErrorNotSupported;
     CUtensorMap xmap;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
+    cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
     cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBN};
     cuuint32_t es[2] = {1, 1};
     if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box,
@@ -322,17 +461,67 @@ cudaError_t run_prefill(float *y, const uint16_t *x, const uint32_t *qw, const u
                                          (int)kSmem);
     if (e != cudaSuccess)
         return e;
+    gemm_prefill_kernel<<<grid, kThreads, kSmem, s>>>(a, xmap);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || a.full == a.tiles)
+        return e;
+    prefill_split_reduce_kernel<<<dim3(a.tiles - a.full, kBN / 32), 256, 0, s>>>(a.y, a.ws, a.M, a.N, a.tiles_n,
+                                                                              a.full, a.S);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+PrefillPlan plan_prefill(int M, int N, int K, int num_sms, size_t ws_floats)
+{
+    // Whole tiles for every full round of the SMs; the tiles of the last,
+    // partial round are split along K into S parts (S = SMs / remaining tiles,
+    // at most 4 and at most the number of k-stages) when the partials fit the
+    // scratch.
+    PrefillPlan p;
+    const int nst = K / kBK;
+    const int tiles = ((N + kBM - 1) / kBM) * ((M + kBN - 1) / kBN);
+    p.full = tiles - tiles % num_sms;
+    const int rem = tiles - p.full;
+    p.S = 1;
+    if (rem > 0) {
+        int S = num_sms / rem;
+        S = S < 4 ? S : 4;
+        S = S < nst ? S : nst;
+        while (S > 1 && (size_t)rem * S * kTileFloats > ws_floats)
+            --S;
+        if (S > 1)
+            p.S = S;
+        else
+            p.full = tiles;
+    }
+    const int items = p.full + (tiles - p.full) * p.S;
+    p.grid = items < num_sms ? items : num_sms;
+    p.bn = kBN;
+    p.ok = true;
+    return p;
+}
+
+cudaError_t run_prefill(const PrefillPlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                        const uint16_t *sc, int M, int N, int K, float *ws, int *err, cudaStream_t s)
+{
+    if (K % kBK != 0 || N % 16 != 0 || !p.ok)
+        return cudaErrorNotSupported;
     PrefillArgs a;
     a.y = y;
     a.qw = qw;
     a.sc = sc;
+    a.ws = ws;
     a.err = err;
     a.M = M;
     a.N = N;
     a.K = K;
-    const dim3 grid((N + kBM - 1) / kBM, (M + kBN - 1) / kBN);
-    gemm_prefill_kernel<<<grid, kThreads, kSmem, s>>>(a, xmap);
-    return cudaGetLastError();
+    a.tiles_n = (N + kBM - 1) / kBM;
+    a.tiles = a.tiles_n * ((M + kBN - 1) / kBN);
+    a.full = p.full;
+    a.S = p.S;
+    a.items = p.full + (a.tiles - p.full) * p.S;
+    return launch(a, x, p.grid, s);
 }
 
 } // namespace w4

@@ -52,8 +52,20 @@ cudaError_t run_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *
 cudaError_t run_read_probe(unsigned long long *sum, const void *buf, size_t bytes, int num_sms,
                            cudaStream_t s);
 
-// Prefill (M > 8) tensor-core GEMM.
-cudaError_t run_prefill(float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int M,
-                        int N, int K, int num_sms, int *err, cudaStream_t s);
+// Prefill (M > 8) tensor-core GEMM: grid persistent CTAs; the first `full`
+// 128x256 tiles whole, the rest split S ways along K and added by a second
+// kernel. ws holds the split partials (128*256 fp32 per split tile and split;
+// capacity ws_floats).
+struct PrefillPlan {
+    int bn = 256;
+    int S = 1;
+    int full = 0;
+    int grid = 1;
+    bool ok = false;
+};
+
+PrefillPlan plan_prefill(int M, int N, int K, int num_sms, size_t ws_floats);
+cudaError_t run_prefill(const PrefillPlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                        const uint16_t *sc, int M, int N, int K, float *ws, int *err, cudaStream_t s);
 
 } // namespace w4
