@@ -205,6 +205,9 @@ gemm_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap xma
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = tmem_base;
+    // The split-K reduction kernel may start launching now; it waits for this
+    // grid to complete before it reads the partials.
+    pdl_launch_dependents();
 
     auto fail = [&]() {
         s_abort = 1;
@@ -328,7 +331,6 @@ gemm_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap xma
     } else {
         // ------------------------------------------------ epilogue
         const int q = warp & 3; // TMEM lane quarter this warp may read
-        const int e = threadIdx.x - kEpiWarp0 * 32;
         uint32_t j = 0;
         for (int i = blockIdx.x; i < a.items; i += gridDim.x, ++j) {
             const Item it = item_of(a, i);
@@ -392,6 +394,7 @@ __global__ void __launch_bounds__(256)
 prefill_split_reduce_kernel(float *__restrict__ y, const float *__restrict__ ws, int M, int N, int tiles_n,
                             int full, int S)
 {
+    pdl_wait(); // the partials are complete and visible
     const int st = blockIdx.x; // split tile index
     const int t = full + st;
     const int n0 = (t % tiles_n) * kBM, m0 = (t / tiles_n) * kBN;
@@ -465,9 +468,20 @@ cudaError_t launch(const PrefillArgs &a, const uint16_t *x, int grid, cudaStream
     e = cudaGetLastError();
     if (e != cudaSuccess || a.full == a.tiles)
         return e;
-    prefill_split_reduce_kernel<<<dim3(a.tiles - a.full, kBN / 32), 256, 0, s>>>(a.y, a.ws, a.M, a.N, a.tiles_n,
-                                                                              a.full, a.S);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the reduction's CTAs are placed while the
+    // GEMM's last tiles finish.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.tiles - a.full, kBN / 32);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_split_reduce_kernel, a.y, (const float *)a.ws, a.M, a.N, a.tiles_n,
+                              a.full, a.S);
 }
 
 } // namespace
