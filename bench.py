@@ -84,7 +84,7 @@ def sweep_weight_bytes() -> int:
 class Sweep:
     """Device-resident sweep: per fused stage one qweight/scales/x/y buffer."""
 
-    def __init__(self, device, keep_host: bool):
+    def __init__(self, device, keep_host: bool, m: int = 1):
         import torch
         self.stages = []
         for l in range(LAYERS):
@@ -97,17 +97,17 @@ class Sweep:
                     synth.gen_qweight_torch(seed_of(l, p), n_p, K, device, out=qw[r:r + n_p])
                     sc_host[r:r + n_p] = synth.gen_scales(seed_of(l, p), n_p, K)
                     r += n_p
-                x_host = synth.gen_x(seed_of(l, members[0]), 1, K)
+                x_host = synth.gen_x(seed_of(l, members[0]), m, K)
                 st = {"layer": l, "name": name, "N": N, "K": K, "qw": qw,
                       "sc": torch.from_numpy(sc_host.view(np.int16)).to(device),
                       "x": torch.from_numpy(x_host.view(np.int16)).to(device),
-                      "y": torch.empty((1, N), dtype=torch.float32, device=device)}
+                      "y": torch.empty((m, N), dtype=torch.float32, device=device)}
                 if keep_host:
                     st["qw_h"] = torch.empty(qw.shape, dtype=torch.int32, pin_memory=True)
                     st["qw_h"].copy_(qw)
                     st["sc_h"] = torch.from_numpy(sc_host.view(np.int16)).pin_memory()
                     st["x_h"] = torch.from_numpy(x_host.view(np.int16)).pin_memory()
-                    st["y_h"] = torch.empty((1, N), dtype=torch.float32, pin_memory=True)
+                    st["y_h"] = torch.empty((m, N), dtype=torch.float32, pin_memory=True)
                 self.stages.append(st)
 
     def run(self, w4, stream=None):
@@ -247,6 +247,115 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def measure_rows(w4, dev, stream):
+    """Per-row measurements beside the sweep (device time, CUDA events on the
+    launching stream; decode calls replayed from a CUDA graph with programmatic
+    dependent launch like the sweep; inputs larger than L2 or rotated through
+    more than L2's worth of copies).
+
+    Returns a dict keyed by row with us per call and GB/s (or TFLOP/s)."""
+    import torch
+    res = {}
+
+    def graph_time(fn, reps=20):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3  # us per replay
+
+    def dev16(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev)
+
+    # Single GEMV 2048x2048, M=1: 64 weight copies (154 MB) rotated.
+    N, K, copies = 2048, 2048, 64
+    qs = [synth.gen_qweight_torch(7000 + c, N, K, dev) for c in range(copies)]
+    sc = dev16(synth.gen_scales(0, N, K))
+    x = dev16(synth.gen_x(0, 1, K))
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    us = graph_time(lambda: [w4.w4a16_gemv(x, q, sc, out=y, stream=stream) for q in qs]) / copies
+    b = stage_bytes(N, K)
+    res["gemv_2048x2048_m1"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    del qs
+
+    # Vocabulary projection 262144x1536 with the fused argmax (226 MB).
+    N, K = 262144, 1536
+    q = synth.gen_qweight_torch(1000, N, K, dev)
+    sc = dev16(synth.gen_scales(1000, N, K))
+    x = dev16(synth.gen_x(1000, 1, K))
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    am = torch.empty((1,), dtype=torch.int32, device=dev)
+    us = graph_time(lambda: w4.w4a16_gemv_argmax(x, q, sc, out=y, argmax=am, stream=stream), reps=10)
+    b = stage_bytes(N, K) + 4
+    res["vocab_argmax_262144x1536"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    del q, sc
+
+    # M=8 decode sweep: the sweep's shapes with 8 x-rows per call.
+    sw8 = Sweep(dev, keep_host=False, m=8)
+    us = graph_time(lambda: sw8.run(w4, stream), reps=10)
+    b = sweep_bytes(8)
+    res["sweep_m8"] = {"us": us, "ms": us / 1e3, "GBps": b / us / 1e3, "bytes": b}
+    del sw8
+
+    # 4-bit row gather: 8 ids from the 262144 x 8960 per-layer table (1.32 GB).
+    N, K = 262144, 8960
+    qt = synth.gen_qweight_torch(2001, N, K, dev)
+    st = dev16(synth.gen_scales(2001, N, K))
+    ids = torch.from_numpy(synth.gen_ids(2002, 8, N).astype(np.int32)).to(dev)
+    out = torch.empty((8, K), dtype=torch.bfloat16, device=dev)
+    us = graph_time(lambda: w4.w4_embed_gather(ids, qt, st, out=out, stream=stream))
+    b = 8 * (K // 2 + K // 16 + 2 * K)
+    res["gather_8x8960"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    del qt, st
+
+    # Prefill GEMM, 1024 tokens, tensor-core bound: 8 weight copies rotated.
+    peak_tf = measured_bf16_peak()
+    for N, K in ((6144, 1536), (1536, 6144)):
+        M = 1024
+        qs = [synth.gen_qweight_torch(3000 + r, N, K, dev) for r in range(8)]
+        sc = dev16(synth.gen_scales(3000, N, K))
+        x = dev16(synth.gen_x(3002, M, K))
+        y = torch.empty((M, N), dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            for r in range(3):
+                w4.w4a16_gemm(x, qs[r], sc, out=y, stream=stream)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for r in range(40):
+                w4.w4a16_gemm(x, qs[r % 8], sc, out=y, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / 40 * 1e3
+        tf = 2.0 * M * N * K / us / 1e6
+        res[f"prefill_{M}x{N}x{K}"] = {"us": us, "TFLOPs": tf, "roofline": {
+            "bound": "tensor", "achieved": tf, "peak": peak_tf[0], "unit": "TFLOP/s", "frac": tf / peak_tf[0],
+            "peak_source": peak_tf[1]}}
+        del qs
+    torch.cuda.empty_cache()
+    return res
+
+
+def measured_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback bf16 burst"
+
+
 def captured_traffic():
     """DRAM bytes (read + write) of one sweep from the committed ncu capture, or
     None when the decode kernel's sources changed after that capture."""
@@ -337,6 +446,8 @@ def run_ours(args, rank, world):
     del probe_buf
     torch.cuda.empty_cache()
 
+    rows = measure_rows(w4, dev, stream) if args.rows else None
+
     # End to end through the public call with host buffers: every step copies
     # the sweep's packed weights, steps and x from pinned host memory and reads
     # every y back. Copies of stage s+1 overlap the GEMV of stage s.
@@ -410,6 +521,7 @@ def run_ours(args, rank, world):
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "kernel": "gemv_m2_kernel (all 140 launches of the sweep)"},
         "probe": {"hbm_read_probe_gbs": probe_gbs, "sweep_frac_of_probe": achieved / probe_gbs},
+        "rows": rows,
         "gpu_launches": ncalls * args.steps,
         "clocks": clk,
         "e2e": e2e,
@@ -466,6 +578,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", dest="rows", action="store_false",
+                    help="skip the per-row measurements (single GEMV, vocabulary argmax, M=8 sweep, "
+                         "gather, prefill)")
     ap.add_argument("--ncu-case", default=None,
                     help="run one small fixed case for an ncu capture instead of the bench: "
                          "decode_shapes | prefill:NxK")
