@@ -126,13 +126,7 @@ int check_w4_args(const void *y, const uint16_t *x, const uint32_t *qw, const ui
 // Shared memory the decode kernels need for x staging; bounded by the SM's 227 KB.
 bool decode_fits(const w4::DecodePlan &p, int M, int K)
 {
-    const int rbc = p.warps / p.ksplit;
-    size_t smem;
-    if (p.kernel == 2)
-        smem = (size_t)M * ((K + 127) / 128 * 128) * 2 + 16 + (size_t)rbc * p.ksplit * M * 64;
-    else
-        smem = (size_t)8 * K * 2 + (size_t)rbc * p.ksplit * 8 * 64;
-    return smem <= 220 * 1024;
+    return w4::decode_smem_bytes(p, M, K) <= 220 * 1024;
 }
 
 // Which decode kernel serves (M, N, K): the tensor-copy streaming kernel where

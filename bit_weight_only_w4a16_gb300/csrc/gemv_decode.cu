@@ -247,6 +247,136 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     }
 }
 
+// ------------------------------------------------------- persistent m2 ----
+//
+// Large N (the vocabulary projection): two resident CTAs of 8 warps per SM,
+// each warp owning every (grid*8)-th 16-row block (ks = 1, whole rows), its
+// k-tiles flattened into one stream so that the 8 tiles in flight run on across
+// row-block boundaries instead of draining and refilling every block (one wave
+// instead of ~7). K % 128 == 0. Same per-tile arithmetic as gemv_m2_kernel.
+template <int MX, int U, bool ARGMAX>
+__global__ void __launch_bounds__(256, 2)
+gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+                       const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc, int N, int K,
+                       unsigned long long *__restrict__ keys)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int nrb = (N + 15) >> 4;
+    const int T = K / kTileK;
+    const int ngroups = K >> 5;
+    const int GW = gridDim.x * 8, gw = blockIdx.x * 8 + warp;
+    const int nmine = nrb > gw ? (nrb - gw + GW - 1) / GW : 0;
+    const int Q = nmine * T; // k-tiles of this warp, row block by row block
+
+    uint4 wa[U], wb[U];
+    uint32_t sa[U], sb[U];
+    int lj = 0, lkt = 0; // loader cursor: row block gw + lj*GW, k-tile lkt
+    auto load = [&](int u) {
+        const int rb = gw + lj * GW;
+        const int rA = min(rb * 16 + g, N - 1), rB = min(rb * 16 + g + 8, N - 1);
+        wa[u] = ldg_stream_v4(qw + (size_t)rA * (K >> 3) + 4 * t + 16 * lkt);
+        wb[u] = ldg_stream_v4(qw + (size_t)rB * (K >> 3) + 4 * t + 16 * lkt);
+        sa[u] = ldg_nc_u32(sc + (size_t)rA * ngroups + 2 * (t & 1) + 4 * lkt);
+        sb[u] = ldg_nc_u32(sc + (size_t)rB * ngroups + 2 * (t & 1) + 4 * lkt);
+        if (++lkt == T) {
+            lkt = 0;
+            ++lj;
+        }
+    };
+
+    if (threadIdx.x == 32)
+        prefetch_l2_bulk(x, (uint32_t)(MX * K * 2));
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (u < Q)
+            load(u);
+    pdl_launch_dependents();
+    pdl_wait();
+
+    uint4 *xs = reinterpret_cast<uint4 *>(smem);
+    const int chunks_per_row = K >> 3;
+    stage_x_rows(xs, x, MX, K, chunks_per_row);
+    uint4 *zero_chunk = xs + MX * chunks_per_row;
+    __shared__ unsigned long long ck[MX];
+    if (threadIdx.x == 0)
+        *zero_chunk = make_uint4(0u, 0u, 0u, 0u);
+    if (ARGMAX && threadIdx.x < MX)
+        ck[threadIdx.x] = 0ull;
+    __syncthreads();
+
+    const int bm = g >> 2;
+    const bool bsel = ((g & 3) == t) && (bm < MX);
+    const uint4 *xrow = bsel ? xs + bm * chunks_per_row + 4 * t : zero_chunk;
+    const int xstep = bsel ? 16 : 0;
+    const int xi = bsel ? 1 : 0;
+    const int m = t >> 1;
+    const bool writer = ((t & 1) == 0) && (m < MX);
+
+    float accA = 0.f, accB = 0.f;
+    int cj = 0, ckt = 0; // compute cursor
+    auto compute = [&](int u) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f}, d[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4 *xb = xrow + xstep * ckt;
+        const uint32_t a_w[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+        const uint32_t b_w[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 b = xb[xi * i];
+            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+            unpack_word(a_w[i], a04, a15, a26, a37);
+            unpack_word(b_w[i], b04, b15, b26, b37);
+            mma_16816(c, a04, b04, a15, b15, b.x, b.y);
+            mma_16816(d, a26, b26, a37, b37, b.z, b.w);
+        }
+        accA = fmaf(bf16lo_to_f32(sa[u]), c[0] + d[0], accA);
+        accA = fmaf(bf16hi_to_f32(sa[u]), c[1] + d[1], accA);
+        accB = fmaf(bf16lo_to_f32(sb[u]), c[2] + d[2], accB);
+        accB = fmaf(bf16hi_to_f32(sb[u]), c[3] + d[3], accB);
+    };
+    auto finish = [&]() {
+        const float a = accA + __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
+        const float b = accB + __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+        const int rowA = (gw + cj * GW) * 16 + g, rowB = rowA + 8;
+        if (writer) {
+            if (rowA < N) {
+                y[(size_t)m * N + rowA] = a;
+                if (ARGMAX)
+                    atomicMax(&ck[m], argmax_key(a, rowA));
+            }
+            if (rowB < N) {
+                y[(size_t)m * N + rowB] = b;
+                if (ARGMAX)
+                    atomicMax(&ck[m], argmax_key(b, rowB));
+            }
+        }
+        accA = accB = 0.f;
+    };
+
+    for (int base = 0; base < Q; base += U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (base + u < Q) {
+                compute(u);
+                if (base + u + U < Q)
+                    load(u);
+                if (++ckt == T) {
+                    finish();
+                    ckt = 0;
+                    ++cj;
+                }
+            }
+        }
+    }
+
+    if (ARGMAX) {
+        __syncthreads();
+        if (threadIdx.x < MX)
+            keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
+    }
+}
+
 // ---------------------------------------------------------------- m8 ----
 
 template <int U, bool ARGMAX>
@@ -446,6 +576,16 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
 {
     DecodePlan p;
     const int nrb = (N + 15) / 16;
+    if (M <= 2 && K % kTileK == 0 && nrb >= 2 * num_sms * 16) {
+        // At least two row blocks per warp of a full single wave: persistent
+        // warps streaming row block after row block.
+        p.kernel = 3;
+        p.ksplit = 1;
+        p.warps = 8;
+        p.unroll = 8;
+        p.grid = 2 * num_sms;
+        return p;
+    }
     if (M <= 2) {
         // Split K until ~12 warps per SM carry the stream, down to one k-tile
         // per warp, as long as the whole grid is resident at once (a second
@@ -532,13 +672,43 @@ static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, c
                       p.ksplit, keys);
 }
 
+size_t decode_smem_bytes(const DecodePlan &p, int M, int K)
+{
+    const size_t rbc = (size_t)(p.warps / p.ksplit);
+    if (p.kernel == 3)
+        return (size_t)M * K * 2 + 16;
+    if (p.kernel == 2)
+        return (size_t)M * ((K + kTileK - 1) / kTileK * kTileK) * 2 + 16 +
+               (p.ksplit > 1 ? rbc * p.ksplit * M * 16 * sizeof(float) : 0);
+    return (size_t)8 * K * 2 + (p.ksplit > 1 ? rbc * p.ksplit * 8 * 16 * sizeof(float) : 0);
+}
+
+template <int MX, bool ARGMAX>
+static cudaError_t launch_persist(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                                  const uint16_t *sc, int N, int K, unsigned long long *keys, cudaStream_t s)
+{
+    const size_t smem = (size_t)MX * K * 2 + 16;
+    auto kern = gemv_m2_persist_kernel<MX, 8, ARGMAX>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    return launch_pdl(kern, dim3(p.grid), dim3(256), smem, s, y, x, qw, sc, N, K, keys);
+}
+
 cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                        const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
                        int32_t *argmax, cudaStream_t s)
 {
     const bool am = argmax != nullptr;
     cudaError_t e;
-    if (p.kernel == 2) {
+    if (p.kernel == 3) {
+        if (M == 1)
+            e = am ? launch_persist<1, true>(p, y, x, qw, sc, N, K, keys, s)
+                   : launch_persist<1, false>(p, y, x, qw, sc, N, K, keys, s);
+        else
+            e = am ? launch_persist<2, true>(p, y, x, qw, sc, N, K, keys, s)
+                   : launch_persist<2, false>(p, y, x, qw, sc, N, K, keys, s);
+    } else if (p.kernel == 2) {
         if (M == 1)
             e = am ? launch_m2<1, true>(p, y, x, qw, sc, N, K, keys, s)
                    : launch_m2<1, false>(p, y, x, qw, sc, N, K, keys, s);

@@ -9,7 +9,8 @@ namespace w4 {
 
 // Per-shape launch plan of the decode kernels (M <= 8).
 struct DecodePlan {
-    int kernel = 2; // 2: M <= 2 kernel (full-group 128-bit loads), 8: M <= 8 kernel
+    int kernel = 2; // 2: M <= 2 kernel (full-group 128-bit loads), 3: its persistent form for
+                    // very large N, 8: M <= 8 kernel
     int ksplit = 1; // warps of a CTA that split K for one 16-row block
     int warps = 8;  // warps per CTA
     int unroll = 4; // k-tiles (m2) or groups (m8) in flight per warp
@@ -17,6 +18,8 @@ struct DecodePlan {
 };
 
 DecodePlan plan_decode(int M, int N, int K, int num_sms);
+// Dynamic shared memory the decode kernel of plan p takes for (M, K).
+size_t decode_smem_bytes(const DecodePlan &p, int M, int K);
 
 // Launches the decode kernel (and, when argmax != nullptr, the argmax pass that
 // reduces keys[M][plan.grid]).

@@ -109,11 +109,7 @@ extern "C" int w4a16_gemv_argmax_noalloc(float *y, int32_t *argmax, const uint16
     // Beyond the fixed scratch: one key per (x-row, CTA).
     if ((long long)M * p.grid > kNoallocKeys)
         return W4_ERR_UNSUPPORTED;
-    const size_t smem = (p.kernel == 2)
-                            ? (size_t)M * ((K + 127) / 128 * 128) * 2 + 16 +
-                                  (size_t)(p.warps / p.ksplit) * p.ksplit * M * 64
-                            : (size_t)8 * K * 2 + (size_t)(p.warps / p.ksplit) * p.ksplit * 8 * 64;
-    if (smem > 220 * 1024)
+    if (w4::decode_smem_bytes(p, M, K) > 220 * 1024)
         return W4_ERR_UNSUPPORTED;
     const cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, d->keys, argmax,
                                          static_cast<cudaStream_t>(stream));

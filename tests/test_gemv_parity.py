@@ -195,6 +195,33 @@ def test_vocab_projection_with_argmax(w4):
     assert int(a[0]) == int(np.argmax(y[0]))
 
 
+@pytest.mark.parametrize("M", [1, 2])
+def test_large_n_sampled_rows_and_argmax(w4, M):
+    # N = 80000 (5000 row blocks: the persistent large-N form on a 152-SM GPU),
+    # K = 1536; logits on sampled rows plus the exact greedy pick per x-row.
+    import torch
+    N, K, seed = 80000, 1536, 1100 + M
+    x = synth.gen_x(seed, M, K)
+    qd = synth.gen_qweight_torch(seed, N, K, "cuda")
+    sc = synth.gen_scales(seed, N, K)
+    y, a = w4.w4a16_gemv_argmax(to_dev_bits16(x), qd, to_dev_bits16(sc))
+    y2 = w4.w4a16_gemv(to_dev_bits16(x), qd, to_dev_bits16(sc))
+    torch.cuda.synchronize()
+    y, a, y2 = y.cpu().numpy(), a.cpu().numpy(), y2.cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, 15, 16, N - 1], rng.integers(0, N, 60)]))
+    qrows = synth.gen_qweight_rows(seed, N, K, rows)
+    yr, ar = oracle.gemm(x, qrows, sc[rows])
+    assert_w4_close(y[:, rows], yr, ar, what=f"large N M{M}")
+    for m in range(M):
+        top = int(np.argmax(y[m]))
+        assert int(a[m]) == int(np.flatnonzero(y[m] == y[m].max())[0]) == top
+        # The picked row agrees with the oracle's value there.
+        yt, at = oracle.gemm(x[m:m + 1], synth.gen_qweight_rows(seed, N, K, np.array([top])), sc[[top]])
+        assert abs(float(y[m, top]) - yt[0, 0]) <= 1e-4 * at[0, 0] + 1e-6
+
+
 def test_streaming_and_register_kernels_agree_with_oracle(w4):
     # Scales that are 4- but not 16-byte aligned route K % 256 == 0 shapes to the
     # register-streaming kernel; aligned ones to the bulk-copy kernel.
