@@ -34,6 +34,13 @@ __device__ __forceinline__ uint32_t ldg_nc_u32(const void *p)
     return v;
 }
 
+__device__ __forceinline__ uint2 ldg_nc_u64(const void *p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t ldg_nc_u16(const void *p)
 {
     unsigned short v;

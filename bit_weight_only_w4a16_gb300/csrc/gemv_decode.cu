@@ -407,6 +407,31 @@ gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 
 // ---------------------------------------------------------------- m8 ----
 
+// 4x4 transpose of 32-bit words across the four lanes of a quad: lane t holds
+// v[j] = W[t][j] on entry and W[j][t] on return (t = lane & 3). Two exchange
+// stages (lane bit 1 with register bit 1, then bit 0 with bit 0), one shuffle
+// per register pair and stage.
+__device__ __forceinline__ void quad_transpose4(uint32_t (&v)[4], int t)
+{
+#pragma unroll
+    for (int bit = 1; bit >= 0; --bit) {
+        const int m = 1 << bit;
+        const bool hi = (t >> bit) & 1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j & m)
+                continue;
+            const int jj = j | m;
+            const uint32_t send = hi ? v[j] : v[jj];
+            const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, send, m);
+            if (hi)
+                v[j] = recv;
+            else
+                v[jj] = recv;
+        }
+    }
+}
+
 template <int U, bool ARGMAX>
 __global__ void __launch_bounds__(512)
 gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
@@ -489,6 +514,156 @@ gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                 compute(u, G0 + base + u);
                 if (base + u + U < nG)
                     load(u, G0 + base + u + U);
+            }
+        }
+    }
+
+    // Lane (g, t) holds y[2t][rowA], y[2t+1][rowA], y[2t][rowB], y[2t+1][rowB].
+    // CTA-best argmax key per x-row; max is order-independent, so deterministic.
+    __shared__ unsigned long long ck[8];
+    if (ARGMAX) {
+        if (threadIdx.x < 8)
+            ck[threadIdx.x] = 0ull;
+        __syncthreads();
+    }
+    const int m0 = 2 * t, m1 = 2 * t + 1;
+    if (ksplit == 1) {
+        if (active) {
+            const float v[2][2] = {{a0, a1}, {b0, b1}};
+            const int rows[2] = {rowA, rowB};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int mm = j ? m1 : m0;
+                    if (rows[h] < N && mm < M) {
+                        y[(size_t)mm * N + rows[h]] = v[h][j];
+                        if (ARGMAX)
+                            atomicMax(&ck[mm], argmax_key(v[h][j], rows[h]));
+                    }
+                }
+            }
+        }
+    } else {
+        float *red = reinterpret_cast<float *>(xs + 8 * cpr); // [rbc][ksplit][8][16]
+        float *r = red + (rbl * ksplit + ks) * 8 * 16;
+        r[m0 * 16 + g] = a0;
+        r[m1 * 16 + g] = a1;
+        r[m0 * 16 + g + 8] = b0;
+        r[m1 * 16 + g + 8] = b1;
+        __syncthreads();
+        for (int i = threadIdx.x; i < rbc * 8 * 16; i += blockDim.x) {
+            const int rr = i & 15, mm = (i >> 4) & 7, rl = i >> 7;
+            const int row = (blockIdx.x * rbc + rl) * 16 + rr;
+            float s = 0.f;
+            for (int k2 = 0; k2 < ksplit; ++k2)
+                s += red[((rl * ksplit + k2) * 8 + mm) * 16 + rr];
+            if (row < N && mm < M) {
+                y[(size_t)mm * N + row] = s;
+                if (ARGMAX)
+                    atomicMax(&ck[mm], argmax_key(s, row));
+            }
+        }
+    }
+    if (ARGMAX) {
+        __syncthreads();
+        if (threadIdx.x < M)
+            keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
+    }
+}
+
+template <int U, bool ARGMAX>
+__global__ void __launch_bounds__(512)
+gemv_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+               const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
+               int M, int N, int K, int ksplit, unsigned long long *__restrict__ keys)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int nwarps = blockDim.x >> 5;
+    const int rbc = nwarps / ksplit;
+    const int ks = warp % ksplit, rbl = warp / ksplit;
+    const int nrb = (N + 15) >> 4;
+    const int rb = blockIdx.x * rbc + rbl;
+    const bool active = rb < nrb;
+    const int ngroups = K >> 5;
+    const int nquads = ngroups >> 2; // 4-group (128-k) units, K % 128 == 0
+    const int Q0 = (int)((long long)nquads * ks / ksplit);
+    const int nQ = (int)((long long)nquads * (ks + 1) / ksplit) - Q0;
+
+    const int rowA = rb * 16 + g, rowB = rowA + 8;
+    const int rA = min(rowA, N - 1), rB = min(rowB, N - 1);
+    // Lane t loads all four words of group 4Q + t (one 128-bit load per row)
+    // and the four steps of the quad's groups; a transpose inside the quad then
+    // gives lane t word t of each of the four groups, as the mma wants.
+    const uint32_t *qA = qw + (size_t)rA * (K >> 3) + 4 * t;
+    const uint32_t *qB = qw + (size_t)rB * (K >> 3) + 4 * t;
+    const uint16_t *sA = sc + (size_t)rA * ngroups;
+    const uint16_t *sB = sc + (size_t)rB * ngroups;
+
+    uint4 wa[U], wb[U];
+    uint2 sa[U], sb[U];
+    auto load = [&](int u, int Q) {
+        wa[u] = ldg_stream_v4(qA + 16 * Q);
+        wb[u] = ldg_stream_v4(qB + 16 * Q);
+        sa[u] = ldg_nc_u64(sA + 4 * Q);
+        sb[u] = ldg_nc_u64(sB + 4 * Q);
+    };
+
+    if (threadIdx.x == 32)
+        prefetch_l2_bulk(x, (uint32_t)(M * K * 2));
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (u < nQ)
+            load(u, Q0 + u);
+    pdl_launch_dependents();
+    pdl_wait();
+
+    uint4 *xs = reinterpret_cast<uint4 *>(smem); // [8][K/8] permuted chunks
+    const int cpr = K >> 3;
+    stage_x_rows(xs, x, M, K, cpr);
+    if (M < 8) // rows M..7 of the B operand are zero
+        for (int i = M * cpr + threadIdx.x; i < 8 * cpr; i += blockDim.x)
+            xs[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+
+    // B column g is x-row g; this lane supplies word t of each group.
+    const uint4 *xrow = xs + g * cpr + t;
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+
+    auto compute = [&](int u, int Q) {
+        uint32_t va[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+        uint32_t vb[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+        quad_transpose4(va, t);
+        quad_transpose4(vb, t);
+        const uint32_t sw_a[2] = {sa[u].x, sa[u].y}, sw_b[2] = {sb[u].x, sb[u].y};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int G = 4 * Q + j;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint4 bx = xrow[4 * G];
+            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+            unpack_word(va[j], a04, a15, a26, a37);
+            unpack_word(vb[j], b04, b15, b26, b37);
+            mma_16816(c, a04, b04, a15, b15, bx.x, bx.y);
+            mma_16816(c, a26, b26, a37, b37, bx.z, bx.w);
+            const float s_a = (j & 1) ? bf16hi_to_f32(sw_a[j >> 1]) : bf16lo_to_f32(sw_a[j >> 1]);
+            const float s_b = (j & 1) ? bf16hi_to_f32(sw_b[j >> 1]) : bf16lo_to_f32(sw_b[j >> 1]);
+            a0 = fmaf(s_a, c[0], a0);
+            a1 = fmaf(s_a, c[1], a1);
+            b0 = fmaf(s_b, c[2], b0);
+            b1 = fmaf(s_b, c[3], b1);
+        }
+    };
+
+    for (int base = 0; base < nQ; base += U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (base + u < nQ) {
+                compute(u, Q0 + base + u);
+                if (base + u + U < nQ)
+                    load(u, Q0 + base + u + U);
             }
         }
     }
@@ -645,15 +820,31 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
         }
         return p;
     } else {
+        // Same rule as M <= 2: split K (down to 4 groups per warp) until ~12
+        // warps per SM carry the stream, while the grid stays one wave.
         const int ngroups = K / 32;
         const int target = num_sms * 12;
-        int ks = 1;
-        while (ks < 16 && (long long)nrb * ks < target && ngroups >= 16 * ks)
-            ks *= 2;
-        p.kernel = 8;
-        p.ksplit = ks;
-        p.warps = ks >= 8 ? ks : 8;
-        p.unroll = 8;
+        auto make = [&](int ks) {
+            DecodePlan q;
+            q.kernel = 8;
+            q.ksplit = ks;
+            q.warps = ks >= 8 ? ks : 8;
+            q.unroll = 8;
+            q.grid = (nrb + q.warps / ks - 1) / (q.warps / ks);
+            return q;
+        };
+        auto resident = [&](const DecodePlan &q) {
+            const int per_sm = (65536 / (96 * 32)) / q.warps;
+            return (long long)q.grid <= (long long)num_sms * per_sm;
+        };
+        p = make(1);
+        for (int ks = 2; ks <= 16 && ngroups >= 4 * ks && (long long)nrb * p.ksplit < target; ks *= 2) {
+            const DecodePlan q = make(ks);
+            if (!resident(q))
+                break;
+            p = q;
+        }
+        return p;
     }
     const int rbc = p.warps / p.ksplit;
     p.grid = (nrb + rbc - 1) / rbc;
@@ -693,6 +884,10 @@ static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, c
     if (p.ksplit > 1)
         smem += (size_t)rbc * p.ksplit * 8 * 16 * sizeof(float);
     auto kern = gemv_m8_kernel<8, ARGMAX>;
+    // 128-bit code loads with a quad transpose when K % 128 == 0 and the steps
+    // allow 8-byte loads.
+    if (K % kTileK == 0 && (reinterpret_cast<uintptr_t>(sc) & 7) == 0)
+        kern = gemv_m8q_kernel<4, ARGMAX>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;

@@ -222,11 +222,12 @@ def test_large_n_sampled_rows_and_argmax(w4, M):
         assert abs(float(y[m, top]) - yt[0, 0]) <= 1e-4 * at[0, 0] + 1e-6
 
 
-def test_streaming_and_register_kernels_agree_with_oracle(w4):
-    # Scales that are 4- but not 16-byte aligned route K % 256 == 0 shapes to the
-    # register-streaming kernel; aligned ones to the bulk-copy kernel.
+@pytest.mark.parametrize("M", [1, 8])
+def test_streaming_and_register_kernels_agree_with_oracle(w4, M):
+    # Steps that are 4- but not 8- or 16-byte aligned take the kernels' narrow-load
+    # paths; aligned ones the wide-load paths. Both agree with the oracle.
     import torch
-    x, qw, sc = synth.gen_w4_problem(77, 1, 500, 1536)
+    x, qw, sc = synth.gen_w4_problem(77, M, 500, 1536)
     yr, ar = oracle.gemm(x, qw, sc)
     xd, qd = to_dev_bits16(x), to_dev_u32(qw)
     flat = torch.zeros(sc.size + 8, dtype=torch.int16, device="cuda")
