@@ -811,6 +811,27 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
             const int per_sm = (65536 / (regs * 32)) / q.warps;
             return (long long)q.grid <= (long long)num_sms * per_sm;
         };
+        if (nrb >= 2 * num_sms) {
+            // Many row blocks: one CTA per SM with ceil(nrb / SMs) row blocks
+            // each, so no SM carries two CTAs' worth of tiles (with 8-warp CTAs
+            // 40 of 152 SMs held two and finished ~2-3 us after the rest), and
+            // K split as far as 16 warps and the register file allow.
+            const int rbc = (nrb + num_sms - 1) / num_sms;
+            for (int ks = 16; ks >= 1; ks /= 2) {
+                if (ks > T || rbc * ks > 16)
+                    continue;
+                const int unroll = (T + ks - 1) / ks > 4 ? 8 : 4;
+                const int regs = unroll == 8 ? 128 : 96;
+                if (rbc * ks * 32 * regs > 65536)
+                    continue;
+                p.kernel = 2;
+                p.ksplit = ks;
+                p.warps = rbc * ks;
+                p.unroll = unroll;
+                p.grid = (nrb + rbc - 1) / rbc;
+                return p;
+            }
+        }
         p = make(1);
         for (int ks = 2; ks <= 16 && ks <= T && (long long)nrb * p.ksplit < target; ks *= 2) {
             const DecodePlan q = make(ks);
