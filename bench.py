@@ -580,6 +580,10 @@ def run_ncu_case(case: str):
 
     decode_shapes : w4a16_gemv, M=1, twice on each of (24576,1536) (1536,12288)
                     (2560,1536), writing a 256 MB buffer between calls.
+    m8_shapes     : the same shapes with M=8.
+    vocab         : w4a16_gemv_argmax twice on the 262144 x 1536 vocabulary projection.
+    gather_probe  : w4_embed_gather of 8 ids from the 262144 x 8960 table and
+                    hbm_read_probe over 1 GiB, twice each.
     prefill:NxK   : w4a16_gemm twice with M=1024 tokens on an N x K weight.
     """
     import torch
@@ -596,7 +600,27 @@ def run_ncu_case(case: str):
         sc = torch.from_numpy(synth.gen_scales(seed, N, K).view(np.int16)).to(dev)
         return x, q, sc
 
-    if case == "decode_shapes":
+    if case == "vocab":
+        x, q, sc = problem(1000, 1, 262144, 1536)
+        for _ in range(2):
+            w4.w4a16_gemv_argmax(x, q, sc)
+    elif case == "m8_shapes":
+        data = [problem(200 + i, 8, N, K) for i, (N, K) in enumerate([(24576, 1536), (1536, 12288), (2560, 1536)])]
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for rep in range(2):
+            for x, q, sc in data:
+                flush.fill_(rep)
+                w4.w4a16_gemv(x, q, sc)
+    elif case == "gather_probe":
+        N, K = 262144, 8960
+        qt = synth.gen_qweight_torch(2001, N, K, dev)
+        st = torch.from_numpy(synth.gen_scales(2001, N, K).view(np.int16)).to(dev)
+        ids = torch.from_numpy(synth.gen_ids(2002, 8, N).astype(np.int32)).to(dev)
+        buf = torch.ones(1 << 28, dtype=torch.int32, device=dev)
+        for _ in range(2):
+            w4.w4_embed_gather(ids, qt, st)
+            w4.hbm_read_probe(buf)
+    elif case == "decode_shapes":
         data = [problem(100 + i, 1, N, K) for i, (N, K) in enumerate([(24576, 1536), (1536, 12288), (2560, 1536)])]
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         for rep in range(2):
@@ -627,7 +651,7 @@ def main():
                          "gather, prefill)")
     ap.add_argument("--ncu-case", default=None,
                     help="run one small fixed case for an ncu capture instead of the bench: "
-                         "decode_shapes | prefill:NxK")
+                         "decode_shapes | m8_shapes | vocab | gather_probe | prefill:NxK")
     args = ap.parse_args()
     if args.ncu_case:
         run_ncu_case(args.ncu_case)
