@@ -44,6 +44,8 @@ def _load():
         lib.w4o_embed_gather.restype = None
         lib.w4o_sum_words.argtypes = [P, I]
         lib.w4o_sum_words.restype = ctypes.c_uint64
+        lib.w4o_attn_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, ctypes.c_double, P]
+        lib.w4o_attn_decode.restype = None
         lib.w4o_f32_to_bf16.argtypes = [ctypes.c_float]
         lib.w4o_f32_to_bf16.restype = ctypes.c_uint16
         _lib = lib
@@ -128,3 +130,28 @@ def sum_words(buf):
 
 def f32_to_bf16(f: float) -> int:
     return int(_load().w4o_f32_to_bf16(float(f)))
+
+
+def attn_decode(q, k, v, kpos=None, qpos=None, window: int = 0, scale: float = 1.0):
+    """(out, absout) fp64 [H][D]: softmax(scale * q k^T) v over the kept cache slots.
+
+    q bf16 bits [H][D]; k, v bf16 bits [T][D]; kpos int32 [T] (recorded position
+    of each slot, -1 = empty) or None (slot t holds position t); qpos defaults to
+    T - 1. absout is sum_t w_t |v_t|, the scale of the parity tolerance.
+    """
+    lib = _load()
+    q = _c(np.atleast_2d(q), np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    H, D = q.shape
+    T = k.shape[0]
+    assert k.shape == (T, D) and v.shape == (T, D)
+    kp = None if kpos is None else _c(kpos, np.int32).ravel()
+    assert kp is None or kp.shape[0] == T
+    qp = T - 1 if qpos is None else int(qpos)
+    out = np.empty((H, D), dtype=np.float64)
+    absout = np.empty((H, D), dtype=np.float64)
+    s = np.empty(max(T, 1), dtype=np.float64)
+    lib.w4o_attn_decode(_ptr(out), _ptr(absout), _ptr(q), _ptr(k), _ptr(v),
+                        None if kp is None else _ptr(kp), qp, int(window), H, T, D, float(scale), _ptr(s))
+    return out, absout

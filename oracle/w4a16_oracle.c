@@ -18,6 +18,14 @@
  *     per-layer row lookup runs on the card.
  *   - The memory-read paragraph: the card's read ceiling is measured by a plain
  *     sum over memory.
+ *   - The decode-attention paragraph: one key/value head serves eight query
+ *     heads; each cached key and value is read once for all of them and the
+ *     result is a softmax over the cached positions, then the values. The
+ *     cache paragraph: full layers keep one slot per position, sliding layers a
+ *     512-slot ring that records each slot's position; "Step 4 - The Model in
+ *     Rust": the ring's attention keeps a slot only if its recorded position is
+ *     >= 0, not after the query's position, and (with a window w) after the
+ *     query's position minus w, then takes the softmax and the values.
  *
  * Readings where the pages are silent (each one is stated where it is used):
  *   R1  8 codes per uint32 along K, low nibble first: code k sits in word k/8 at
@@ -27,6 +35,9 @@
  *   R3  The gather output is bf16, round-to-nearest-even of the exact product.
  *   R4  Argmax is the lowest index of the largest value; -0 equals +0.
  *   R5  The read probe's result is the sum of all 32-bit words mod 2^64.
+ *   R6  Attention scores are scale * (q . k) with the scale an argument (the
+ *       pages' listing multiplies q by k^T and names no scale); a query with no
+ *       kept slot gives a zero output.
  *
  * Parity pins: every function here is pinned by the not-gpu tests (hand-worked
  * examples with the packed words written in hex, closed forms, invariants, and
@@ -180,3 +191,57 @@ uint64_t w4o_sum_words(const uint32_t *buf, int64_t nwords)
 
 /* Exposed for the pins on rounding: binary32 -> bf16 bits, RNE. */
 uint16_t w4o_f32_to_bf16(float f) { return float_to_bf16_rne(f); }
+
+/*
+ * Decode attention for one query token (R6), in fp64, the plain definition:
+ *   s[h][t] = scale * sum_d q[h][d] * k[t][d]            for kept slots t
+ *   w[h][t] = exp(s[h][t] - max_t s[h][t]) / sum_t exp(...)
+ *   out[h][d] = sum_t w[h][t] * v[t][d],  absout[h][d] = sum_t w[h][t] * |v[t][d]|
+ * Slot t records position kpos[t] (kpos == NULL: position t). It is kept iff
+ * kpos[t] >= 0, kpos[t] <= qpos and, when window > 0, kpos[t] > qpos - window.
+ * q is bf16 bits [H][D]; k and v are bf16 bits [T][D] (one key/value head).
+ * s is caller scratch of T doubles.
+ */
+void w4o_attn_decode(double *out, double *absout, const uint16_t *q, const uint16_t *k,
+                     const uint16_t *v, const int32_t *kpos, int64_t qpos, int64_t window,
+                     int64_t H, int64_t T, int64_t D, double scale, double *s)
+{
+    for (int64_t h = 0; h < H; ++h) {
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t p = kpos ? (int64_t)kpos[t] : t;
+            int keep = p >= 0 && p <= qpos && (window <= 0 || p > qpos - window);
+            if (!keep) {
+                s[t] = -INFINITY;
+                continue;
+            }
+            double acc = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                acc += bf16_to_double(q[h * D + d]) * bf16_to_double(k[t * D + d]);
+            s[t] = scale * acc;
+            if (s[t] > mx)
+                mx = s[t];
+        }
+        for (int64_t d = 0; d < D; ++d) {
+            out[h * D + d] = 0.0;
+            absout[h * D + d] = 0.0;
+        }
+        if (mx == -INFINITY)
+            continue;
+        double z = 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            s[t] = (s[t] == -INFINITY) ? 0.0 : exp(s[t] - mx);
+            z += s[t];
+        }
+        for (int64_t t = 0; t < T; ++t) {
+            if (s[t] == 0.0)
+                continue;
+            double w = s[t] / z;
+            for (int64_t d = 0; d < D; ++d) {
+                double vv = bf16_to_double(v[t * D + d]);
+                out[h * D + d] += w * vv;
+                absout[h * D + d] += w * fabs(vv);
+            }
+        }
+    }
+}

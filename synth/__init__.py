@@ -19,7 +19,12 @@ Rounding of generated values: fp64 -> fp32 (round to nearest even) -> bf16 (roun
 to nearest even). The bf16 bits are the data; both sides consume the same bits.
 
 Stream state: seed * 0x9E3779B97F4A7C15 + tag (mod 2^64), with tag 0 = codes,
-1 = steps, 2 = x (one row), 3 = ids, 4 = x (several rows), 5 = probe buffer.
+1 = steps, 2 = x (one row), 3 = ids, 4 = x (several rows), 5 = probe buffer,
+6 = attention query, 7 = cached keys, 8 = cached values.
+
+Attention inputs (decode attention over a one-head key/value cache): q, keys and
+values bf16(N(0,1)); the ring of a sliding layer holds the last `slots` positions
+up to the query's (slot j = position p with p % slots == j), empty slots -1.
 """
 from __future__ import annotations
 
@@ -30,6 +35,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 TAG_CODES, TAG_STEPS, TAG_X, TAG_IDS, TAG_XROWS, TAG_PROBE = 0, 1, 2, 3, 4, 5
+TAG_Q, TAG_K, TAG_V = 6, 7, 8
 
 _CHUNK = 1 << 20
 _S27, _S30, _S31 = np.uint64(27), np.uint64(30), np.uint64(31)
@@ -159,6 +165,25 @@ def gen_words(seed: int, nwords: int) -> np.ndarray:
     """uint32 [nwords] of uniform bits (buffer for the memory read probe)."""
     w = splitmix64(stream_state(seed, TAG_PROBE), 0, nwords)
     return (w & np.uint64(0xFFFFFFFF)).astype(np.uint32)
+
+
+def gen_attn_q(seed: int, heads: int, d: int) -> np.ndarray:
+    """bf16 bits [heads][d], N(0,1)."""
+    return f64_to_bf16_bits(normals(stream_state(seed, TAG_Q), heads * d)).reshape(heads, d)
+
+
+def gen_attn_kv(seed: int, slots: int, d: int, start: int = 0):
+    """(k, v) bf16 bits [slots][d], N(0,1); rows start .. start+slots-1 of the streams."""
+    k = f64_to_bf16_bits(normals(stream_state(seed, TAG_K), slots * d, start * d)).reshape(slots, d)
+    v = f64_to_bf16_bits(normals(stream_state(seed, TAG_V), slots * d, start * d)).reshape(slots, d)
+    return k, v
+
+
+def ring_positions(qpos: int, slots: int) -> np.ndarray:
+    """int32 [slots]: the position each ring slot records after writing 0..qpos (-1 = empty)."""
+    j = np.arange(slots, dtype=np.int64)
+    p = qpos - ((qpos - j) % slots)
+    return np.where(p >= 0, p, -1).astype(np.int32)
 
 
 def gen_w4_problem(seed: int, m: int, n: int, k: int, group: int = 32):
