@@ -353,6 +353,35 @@ def measure_rows(w4, dev, stream):
     res["gather_8x8960"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
     del qt, st
 
+    # Decode attention over a one-head key/value cache (8 query heads): the
+    # full-length layer at 131072 slots x 512 (256 MiB of keys and values per
+    # call, larger than L2) and the sliding layer's 512-slot ring x 256 (512 KB,
+    # rotated through 512 copies).
+    hbm = measured_peaks()[0]
+    H, T, D = 8, 131072, 512
+    q = dev16(synth.gen_attn_q(404, H, D))
+    kh, vh = synth.gen_attn_kv(404, T, D)
+    k, v = dev16(kh), dev16(vh)
+    del kh, vh
+    out = torch.empty((H, D), dtype=torch.float32, device=dev)
+    us = graph_time(lambda: w4.w4_attn_decode(q, k, v, scale=D ** -0.5, out=out, stream=stream))
+    b = 2 * T * D * 2 + H * D * 2 + H * D * 4
+    res["attn_full_131072x512"] = {"us": us, "GBps": b / us / 1e3, "bytes": b,
+                                   "frac_of_copy_peak": b / us / 1e3 / hbm}
+    del k, v
+    H, T, D, copies, qpos = 8, 512, 256, 512, 70000
+    q = dev16(synth.gen_attn_q(405, H, D))
+    kh, vh = synth.gen_attn_kv(405, T, D)
+    k1, v1 = dev16(kh), dev16(vh)
+    ks = [k1.clone() for _ in range(copies)]
+    vs = [v1.clone() for _ in range(copies)]
+    kp = torch.from_numpy(synth.ring_positions(qpos, T)).to(dev)
+    us = graph_time(lambda: [w4.w4_attn_decode(q, ks[c], vs[c], kp, qpos=qpos, window=T, scale=D ** -0.5,
+                                               out=out, stream=stream) for c in range(copies)], reps=5) / copies
+    b = 2 * T * D * 2 + H * D * 2 + H * D * 4 + T * 4
+    res["attn_ring_512x256"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    del ks, vs, k1, v1
+
     # Prefill GEMM, 1024 tokens, tensor-core bound: 8 weight copies rotated.
     peak_tf = measured_bf16_peak()
     for N, K in ((6144, 1536), (1536, 6144)):
@@ -584,6 +613,7 @@ def run_ncu_case(case: str):
     vocab         : w4a16_gemv_argmax twice on the 262144 x 1536 vocabulary projection.
     gather_probe  : w4_embed_gather of 8 ids from the 262144 x 8960 table and
                     hbm_read_probe over 1 GiB, twice each.
+    attn          : w4_attn_decode twice over a 131072-slot x 512 cache (8 heads).
     prefill:NxK   : w4a16_gemm twice with M=1024 tokens on an N x K weight.
     """
     import torch
@@ -600,7 +630,15 @@ def run_ncu_case(case: str):
         sc = torch.from_numpy(synth.gen_scales(seed, N, K).view(np.int16)).to(dev)
         return x, q, sc
 
-    if case == "vocab":
+    if case == "attn":
+        H, T, D = 8, 131072, 512
+        q = torch.from_numpy(synth.gen_attn_q(404, H, D).view(np.int16)).to(dev)
+        kh, vh = synth.gen_attn_kv(404, T, D)
+        k = torch.from_numpy(kh.view(np.int16)).to(dev)
+        v = torch.from_numpy(vh.view(np.int16)).to(dev)
+        for _ in range(2):
+            w4.w4_attn_decode(q, k, v, scale=D ** -0.5)
+    elif case == "vocab":
         x, q, sc = problem(1000, 1, 262144, 1536)
         for _ in range(2):
             w4.w4a16_gemv_argmax(x, q, sc)
@@ -651,7 +689,7 @@ def main():
                          "gather, prefill)")
     ap.add_argument("--ncu-case", default=None,
                     help="run one small fixed case for an ncu capture instead of the bench: "
-                         "decode_shapes | m8_shapes | vocab | gather_probe | prefill:NxK")
+                         "decode_shapes | m8_shapes | vocab | gather_probe | attn | prefill:NxK")
     args = ap.parse_args()
     if args.ncu_case:
         run_ncu_case(args.ncu_case)

@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED",
 
 # Symbols declared in include/w4a16.h.
 EXPORTS = ("w4_status_string", "w4_last_cuda_error", "w4_init", "w4_device_error", "w4a16_gemv", "w4a16_gemm",
-           "w4a16_gemv_argmax", "w4a16_gemv_argmax_noalloc", "w4_embed_gather", "hbm_read_probe")
+           "w4a16_gemv_argmax", "w4a16_gemv_argmax_noalloc", "w4_embed_gather", "hbm_read_probe",
+           "w4_attn_decode")
 
 
 class W4Error(RuntimeError):
@@ -60,6 +61,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_embed_gather.restype = I
     lib.hbm_read_probe.argtypes = [P, P, S, P]
     lib.hbm_read_probe.restype = I
+    lib.w4_attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_float, P]
+    lib.w4_attn_decode.restype = I
     return lib
 
 
@@ -190,3 +193,26 @@ def hbm_read_probe(buf, out=None, stream=None):
     s = torch.empty((1,), dtype=torch.int64, device=buf.device) if out is None else _cuda(out, "out")
     _check(_lib.hbm_read_probe(_ptr(s), _ptr(buf), nbytes, _stream(stream)), "hbm_read_probe")
     return s
+
+
+def w4_attn_decode(q, k, v, kpos=None, qpos=None, window: int = 0, scale: float = 1.0, out=None, stream=None):
+    """fp32 [H][D]: softmax(scale * q k^T) v over the kept slots of a one-head cache.
+
+    q bf16 [H][D] (H <= 8 query heads sharing the key/value head); k, v bf16 [T][D];
+    kpos int32 [T] (position recorded in each slot, -1 = empty) or None (slot t
+    holds position t); qpos defaults to T - 1; window 0 = no window.
+    """
+    _bits16(q, "q"); _bits16(k, "k"); _bits16(v, "v")
+    H, D = q.shape
+    T = k.shape[0]
+    if tuple(k.shape) != (T, D) or tuple(v.shape) != (T, D):
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if kpos is not None:
+        _cuda(kpos, "kpos")
+        if kpos.dtype != torch.int32 or kpos.numel() != T:
+            raise ValueError("kpos must be int32 [T]")
+    qp = T - 1 if qpos is None else int(qpos)
+    o = torch.empty((H, D), dtype=torch.float32, device=q.device) if out is None else _cuda(out, "out")
+    _check(_lib.w4_attn_decode(_ptr(o), _ptr(q), _ptr(k), _ptr(v), _ptr(kpos), qp, int(window), H, T, D,
+                               float(scale), _stream(stream)), "w4_attn_decode")
+    return o

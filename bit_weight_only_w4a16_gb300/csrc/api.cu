@@ -304,4 +304,28 @@ int hbm_read_probe(unsigned long long *sum, const void *buf, size_t bytes, void 
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 
+int w4_attn_decode(float *out, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                   const int32_t *kpos, int qpos, int window, int H, int T, int D, float scale,
+                   void *stream)
+{
+    if (!out || !q || !k || !v)
+        return W4_ERR_INVALID_ARG;
+    if (H < 1 || T < 1 || D < 1 || window < 0)
+        return W4_ERR_INVALID_ARG;
+    if (H > 8 || D % 128 != 0 || D > 512)
+        return W4_ERR_UNSUPPORTED;
+    if ((long long)T * D >= (1ll << 31))
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 4) ||
+        (kpos && !aligned(kpos, 4)))
+        return W4_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != W4_OK)
+        return rc;
+    cudaError_t e = w4::run_attn_decode(out, q, k, v, kpos, qpos, window, H, T, D, scale, st->ws, kWsFloats,
+                                        st->num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
 } // extern "C"

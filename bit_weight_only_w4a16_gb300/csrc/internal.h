@@ -71,4 +71,10 @@ PrefillPlan plan_prefill(int M, int N, int K, int num_sms, size_t ws_floats);
 cudaError_t run_prefill(const PrefillPlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                         const uint16_t *sc, int M, int N, int K, float *ws, int *err, cudaStream_t s);
 
+// Decode attention of one query token (H <= 8 query heads sharing one key/value
+// head, D in {128, 256, 384, 512}) over T cache slots; split partials in ws.
+cudaError_t run_attn_decode(float *out, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const int32_t *kpos, long long qpos, long long window, int H, int T, int D,
+                            float scale, float *ws, size_t ws_floats, int num_sms, cudaStream_t s);
+
 } // namespace w4

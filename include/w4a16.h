@@ -148,6 +148,36 @@ int w4_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qtable,
  */
 int hbm_read_probe(unsigned long long *sum, const void *buf, size_t bytes, void *stream);
 
+/*
+ * Decode attention of one query token over a one-head key/value cache (source:
+ * "Gemma 4 E2B on a 4 GB GPU with pure PyTorch", decode-attention paragraph: one
+ * key/value head serves eight query heads and each cached key and value is read
+ * once for all of them, the cache split into slices combined with an online
+ * softmax; cache paragraph: full layers keep one slot per position, sliding
+ * layers a ring that records each slot's position; "Step 4 - The Model in
+ * Rust": a slot is kept iff its position p satisfies p >= 0, p <= qpos and,
+ * when window > 0, p > qpos - window).
+ *
+ *   out[h][d] = sum_t w[h][t] * v[t][d],  w[h][.] = softmax over kept slots t of
+ *               scale * sum_d q[h][d] * k[t][d]
+ *
+ *   out    fp32 [H][D] (4-byte aligned); a head with no kept slot gives zeros
+ *   q      bf16 [H][D] query heads sharing the key/value head (16-byte aligned)
+ *   k, v   bf16 [T][D] cache slots, slot-major (16-byte aligned)
+ *   kpos   int32 [T] position recorded in each slot (-1 = empty), or NULL:
+ *          slot t holds position t (a full-length cache)
+ *   qpos   the query's position; window 0 = no window
+ *   H in 1..8, T >= 1, D in {128, 256, 384, 512}, T * D < 2^31.
+ * Precision: bf16 x bf16 products accumulated in fp32 for the scores; the
+ * softmax weights are rounded to bf16 for the value product (and the
+ * normalising sum adds the rounded weights); fp32 accumulation; results are
+ * deterministic. Uses the library's split scratch (like w4a16_gemm): calls that
+ * need it must not run concurrently on different streams.
+ */
+int w4_attn_decode(float *out, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                   const int32_t *kpos, int qpos, int window, int H, int T, int D, float scale,
+                   void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -78,6 +78,17 @@ def test_validation_before_any_launch(lib):
     # prefill shape rules
     assert l.w4a16_gemm(A, A, A, A, 64, 24, 64, 32, None) == 2
     assert l.w4a16_gemm(A, A, A, A, 64, 32, 96, 32, None) == 2
+    # decode attention: NULL, sizes, head count / width, alignment
+    f = ctypes.c_float(1.0)
+    assert l.w4_attn_decode(None, A, A, A, None, 0, 0, 8, 16, 512, f, None) == 1
+    assert l.w4_attn_decode(A, A, A, A, None, 0, 0, 8, 0, 512, f, None) == 1
+    assert l.w4_attn_decode(A, A, A, A, None, 0, -1, 8, 16, 512, f, None) == 1
+    assert l.w4_attn_decode(A, A, A, A, None, 0, 0, 9, 16, 512, f, None) == 2
+    assert l.w4_attn_decode(A, A, A, A, None, 0, 0, 8, 16, 200, f, None) == 2
+    assert l.w4_attn_decode(A, A, A, A, None, 0, 0, 8, 16, 1024, f, None) == 2
+    assert l.w4_attn_decode(A, A, _addr((1 << 20) + 8), A, None, 0, 0, 8, 16, 512, f, None) == 3
+    assert l.w4_attn_decode(A, A, A, A, _addr((1 << 20) + 2), 0, 0, 8, 16, 512, f, None) == 3
+    assert l.w4_attn_decode(A, A, A, A, None, 0, 0, 8, 1 << 22, 512, f, None) == 1
 
 
 def test_no_device_reported_without_gpu(lib):
