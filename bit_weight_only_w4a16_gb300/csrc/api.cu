@@ -110,7 +110,7 @@ int check_w4_args(const void *y, const uint16_t *x, const uint32_t *qw, const ui
         return W4_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0)
         return W4_ERR_INVALID_ARG;
-    if (group != 32)
+    if (w4::group_shift(group) < 0)
         return W4_ERR_UNSUPPORTED;
     if (K % group != 0)
         return W4_ERR_INVALID_ARG;
@@ -179,7 +179,8 @@ int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (use_stream(M, N, K, qweight, scales)) {
+    const int lg = w4::group_shift(group);
+    if (lg == 0 && use_stream(M, N, K, qweight, scales)) {
         const w4::StreamPlan sp = w4::plan_stream(M, N, K, st->num_sms);
         if (sp.ok) {
             cudaError_t e = w4::run_stream(sp, y, x, qweight, scales, M, N, K, nullptr, nullptr,
@@ -190,7 +191,7 @@ int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
     const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
     if (!decode_fits(p, M, K))
         return W4_ERR_UNSUPPORTED;
-    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, nullptr, nullptr, s);
+    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, lg, nullptr, nullptr, s);
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 
@@ -208,7 +209,7 @@ int w4a16_gemm(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
     const w4::PrefillPlan p = w4::plan_prefill(M, N, K, st->num_sms, kWsFloats);
-    cudaError_t e = w4::run_prefill(p, y, x, qweight, scales, M, N, K, st->ws, st->err,
+    cudaError_t e = w4::run_prefill(p, y, x, qweight, scales, M, N, K, w4::group_shift(group), st->ws, st->err,
                                     static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported)
         return W4_ERR_UNSUPPORTED;
@@ -231,7 +232,8 @@ int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (use_stream(M, N, K, qweight, scales)) {
+    const int lg = w4::group_shift(group);
+    if (lg == 0 && use_stream(M, N, K, qweight, scales)) {
         const w4::StreamPlan sp = w4::plan_stream(M, N, K, st->num_sms);
         if (sp.ok && (size_t)M * sp.C * sp.nclusters <= kKeyCapacity) {
             cudaError_t e = w4::run_stream(sp, y, x, qweight, scales, M, N, K, st->keys, argmax,
@@ -242,7 +244,7 @@ int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32
     const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
     if (!decode_fits(p, M, K) || (size_t)M * p.grid > kKeyCapacity)
         return W4_ERR_UNSUPPORTED;
-    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, st->keys, argmax, s);
+    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, lg, st->keys, argmax, s);
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 
@@ -254,7 +256,7 @@ int w4_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qtable,
         return W4_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0)
         return W4_ERR_INVALID_ARG;
-    if (group != 32)
+    if (w4::group_shift(group) < 0)
         return W4_ERR_UNSUPPORTED;
     if (K % group != 0)
         return W4_ERR_INVALID_ARG;
@@ -267,7 +269,7 @@ int w4_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qtable,
     int rc = device_state(&st);
     if (rc != W4_OK)
         return rc;
-    cudaError_t e = w4::run_embed_gather(out, ids, qtable, scales, M, N, K, status,
+    cudaError_t e = w4::run_embed_gather(out, ids, qtable, scales, M, N, K, w4::group_shift(group), status,
                                          static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }

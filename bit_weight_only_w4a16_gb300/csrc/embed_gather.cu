@@ -31,12 +31,12 @@ __device__ __forceinline__ uint32_t bf16x2_of_codes(uint32_t w, int shift, float
 __global__ void __launch_bounds__(256)
 embed_gather_kernel(uint16_t *__restrict__ out, const int32_t *__restrict__ ids,
                     const uint32_t *__restrict__ qt, const uint16_t *__restrict__ sc, int M,
-                    int N, int K, int32_t *__restrict__ status)
+                    int N, int K, int lg, int32_t *__restrict__ status)
 {
     pdl_launch_dependents();
     pdl_wait();
     const int words = K >> 3;
-    const int ngroups = K >> 5;
+    const int nsteps = K >> (5 + lg); // one step per 32 << lg codes
     const long long total = (long long)M * words;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
@@ -46,7 +46,7 @@ embed_gather_kernel(uint16_t *__restrict__ out, const int32_t *__restrict__ ids,
         uint4 o = make_uint4(0u, 0u, 0u, 0u);
         if (id >= 0 && id < N) {
             const uint32_t w = qt[(size_t)id * words + wd];
-            const float s = bf16lo_to_f32(sc[(size_t)id * ngroups + (wd >> 2)]);
+            const float s = bf16lo_to_f32(sc[(size_t)id * nsteps + ((wd >> 2) >> lg)]);
             // codes 0..7 of the word are k = 8*wd + 0..7, low nibble first
             o.x = bf16x2_of_codes(w, 0, s);
             o.y = bf16x2_of_codes(w, 8, s);
@@ -60,7 +60,7 @@ embed_gather_kernel(uint16_t *__restrict__ out, const int32_t *__restrict__ ids,
 }
 
 cudaError_t run_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qt,
-                             const uint16_t *sc, int M, int N, int K, int32_t *status,
+                             const uint16_t *sc, int M, int N, int K, int lg, int32_t *status,
                              cudaStream_t s)
 {
     const long long total = (long long)M * (K >> 3);
@@ -76,7 +76,7 @@ cudaError_t run_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, embed_gather_kernel, out, ids, qt, sc, M, N, K, status);
+    return cudaLaunchKernelEx(&cfg, embed_gather_kernel, out, ids, qt, sc, M, N, K, lg, status);
 }
 
 } // namespace w4

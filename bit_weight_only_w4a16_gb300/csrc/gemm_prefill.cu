@@ -8,7 +8,7 @@
 // dequantized on their way into shared memory and never exist as a 16-bit copy
 // in HBM.
 //
-// y[m][n] = sum_k x[m][k] * bf16_rne((code(n,k) - 8) * step(n, k/32)), fp32
+// y[m][n] = sum_k x[m][k] * bf16_rne((code(n,k) - 8) * step(n, k/group)), fp32
 // accumulate. Rounding each weight to bf16 (relative error <= 2^-9) keeps the
 // result within 2e-3 * sum|w x|.
 //
@@ -137,6 +137,7 @@ struct PrefillArgs {
     float *ws; // split partials, one kTileFloats slot per (split tile, split)
     int *err;
     int M, N, K;
+    int lg;       // one step per 32 << lg codes
     int tiles_n;  // 128-row weight tiles
     int tiles;    // tiles_n * 256-token tiles
     int full;     // tiles computed whole (the first full rounds)
@@ -278,7 +279,7 @@ gemm_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap xma
             const int n = (it.t % a.tiles_n) * kBM + r;
             const bool valid = n < a.N;
             const uint32_t *qrow = a.qw + (size_t)(valid ? n : 0) * (a.K >> 3) + 4 * h;
-            const uint16_t *srow = a.sc + (size_t)(valid ? n : 0) * (a.K >> 5) + h;
+            const uint16_t *srow = a.sc + (size_t)(valid ? n : 0) * (a.K >> (5 + a.lg));
             // Codes and step of the next kDqAhead stages in flight: stage st lives
             // in register set (st - k0) % kDqAhead, refilled with st + kDqAhead as
             // soon as it is consumed (no register copies, which would wait for the
@@ -288,7 +289,7 @@ gemm_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap xma
             auto load = [&](int st, uint4 &w, uint32_t &s1) {
                 if (valid && st < k1) {
                     w = ldg_stream_v4(qrow + 8 * st);
-                    s1 = ldg_nc_u16(srow + 2 * st);
+                    s1 = ldg_nc_u16(srow + ((2 * st + h) >> a.lg));
                 } else {
                     w = make_uint4(0u, 0u, 0u, 0u);
                     s1 = 0u;
@@ -517,7 +518,7 @@ PrefillPlan plan_prefill(int M, int N, int K, int num_sms, size_t ws_floats)
 }
 
 cudaError_t run_prefill(const PrefillPlan &p, float *y, const uint16_t *x, const uint32_t *qw,
-                        const uint16_t *sc, int M, int N, int K, float *ws, int *err, cudaStream_t s)
+                        const uint16_t *sc, int M, int N, int K, int lg, float *ws, int *err, cudaStream_t s)
 {
     if (K % kBK != 0 || N % 16 != 0 || !p.ok)
         return cudaErrorNotSupported;
@@ -525,6 +526,7 @@ cudaError_t run_prefill(const PrefillPlan &p, float *y, const uint16_t *x, const
     a.y = y;
     a.qw = qw;
     a.sc = sc;
+    a.lg = lg;
     a.ws = ws;
     a.err = err;
     a.M = M;

@@ -66,16 +66,29 @@ __device__ __forceinline__ void stage_x_rows(uint4 *xs, const uint16_t *x, int r
     }
 }
 
+// The steps of the 32-code groups j and j + 1 (j even) of one row as a bf16
+// pair, low half first. Rows hold one step per 32 << lg codes, so for lg >= 1
+// both groups share a step. G32 (lg == 0 known at compile time) keeps the
+// group-32 path free of the test.
+template <bool G32>
+__device__ __forceinline__ uint32_t step_pair(const uint16_t *srow, int j, int lg)
+{
+    if (G32 || lg == 0)
+        return ldg_nc_u32(srow + j);
+    const uint32_t v = ldg_nc_u16(srow + (j >> lg));
+    return v | (v << 16);
+}
+
 // ---------------------------------------------------------------- m2 ----
 
 // FULL (K % 128 == 0, implies SC32): every k-tile is whole, so the loads need
 // no per-group guards; warps past the last row block load clamped rows and
 // never store.
-template <int MX, int U, bool SC32, bool FULL, bool ARGMAX>
+template <int MX, int U, bool SC32, bool FULL, bool ARGMAX, bool G32>
 __global__ void __launch_bounds__(512)
 gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
-               int N, int K, int ksplit, unsigned long long *__restrict__ keys)
+               int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -96,8 +109,13 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     const int rA = min(rowA, N - 1), rB = min(rowB, N - 1);
     const uint32_t *qA = qw + (size_t)rA * (K >> 3) + 4 * t;
     const uint32_t *qB = qw + (size_t)rB * (K >> 3) + 4 * t;
-    const uint16_t *sA = sc + (size_t)rA * ngroups + 2 * (t & 1);
-    const uint16_t *sB = sc + (size_t)rB * ngroups + 2 * (t & 1);
+    // Steps: one per 32 << lg codes, K >> (5 + lg) per row. This lane scales
+    // the 32-code groups 4kt + jt and 4kt + jt + 1 (one pair).
+    const int sstride = G32 ? ngroups : (ngroups >> lg);
+    const uint16_t *sA = sc + (size_t)rA * sstride;
+    const uint16_t *sB = sc + (size_t)rB * sstride;
+    const int jt = 2 * (t & 1);
+    const uint16_t *sAj = sA + jt, *sBj = sB + jt; // group 32: this lane's pair
 
     uint4 wa[U], wb[U];
     uint32_t sa[U], sb[U];
@@ -106,8 +124,13 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         if (FULL) {
             wa[u] = ldg_stream_v4(qA + 16 * kt);
             wb[u] = ldg_stream_v4(qB + 16 * kt);
-            sa[u] = ldg_nc_u32(sA + 4 * kt);
-            sb[u] = ldg_nc_u32(sB + 4 * kt);
+            if (G32) {
+                sa[u] = ldg_nc_u32(sAj + 4 * kt);
+                sb[u] = ldg_nc_u32(sBj + 4 * kt);
+            } else {
+                sa[u] = step_pair<false>(sA, 4 * kt + jt, lg);
+                sb[u] = step_pair<false>(sB, 4 * kt + jt, lg);
+            }
             return;
         }
         const int G = 4 * kt + t;
@@ -121,12 +144,12 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         const int Gs = 4 * kt + 2 * (t & 1);
         if (SC32) {
             const bool ok = active && Gs < ngroups;
-            sa[u] = ok ? ldg_nc_u32(sA + 4 * kt) : 0u;
-            sb[u] = ok ? ldg_nc_u32(sB + 4 * kt) : 0u;
-        } else {
+            sa[u] = ok ? step_pair<G32>(sA, Gs, lg) : 0u;
+            sb[u] = ok ? step_pair<G32>(sB, Gs, lg) : 0u;
+        } else { // K % 64 != 0, so the group is 32 (lg == 0)
             const bool ok0 = active && Gs < ngroups, ok1 = active && Gs + 1 < ngroups;
-            sa[u] = (ok0 ? ldg_nc_u16(sA + 4 * kt) : 0u) | ((ok1 ? ldg_nc_u16(sA + 4 * kt + 1) : 0u) << 16);
-            sb[u] = (ok0 ? ldg_nc_u16(sB + 4 * kt) : 0u) | ((ok1 ? ldg_nc_u16(sB + 4 * kt + 1) : 0u) << 16);
+            sa[u] = (ok0 ? ldg_nc_u16(sA + Gs) : 0u) | ((ok1 ? ldg_nc_u16(sA + Gs + 1) : 0u) << 16);
+            sb[u] = (ok0 ? ldg_nc_u16(sB + Gs) : 0u) | ((ok1 ? ldg_nc_u16(sB + Gs + 1) : 0u) << 16);
         }
     };
 
@@ -258,11 +281,11 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 // 59.0 -> 48.9 us for a 262144 x 1536 GEMV against one tile at a time with
 // addresses recomputed per load; 4 tiles in flight per warp (105 registers)
 // then beat 6, 8 or 12 (46.3 vs 48.1, 49.0, 63.0 us) and 3 or 4 CTAs per SM.
-template <int MX, int U, int MINB, bool ARGMAX>
+template <int MX, int U, int MINB, bool ARGMAX, bool G32>
 __global__ void __launch_bounds__(256, MINB)
 gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                        const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc, int N, int K,
-                       unsigned long long *__restrict__ keys)
+                       unsigned long long *__restrict__ keys, int lg)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -279,22 +302,27 @@ gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     // Loader pointers (N % 16 == 0: no clamped rows): row A of the warp's
     // current row block at its current k-tile; row B is 8 rows (K words) on.
     const uint32_t *lp = qw + (size_t)(gw * 16 + g) * (K >> 3) + 4 * t;
-    const uint16_t *ls = sc + (size_t)(gw * 16 + g) * ngroups + 2 * (t & 1);
+    // Step row of row A and this lane's 32-code group index in it (steps: one
+    // per 32 << lg codes).
+    const int sstride = ngroups >> lg;
+    const uint16_t *ls = sc + (size_t)(gw * 16 + g) * sstride;
+    int lj = 2 * (t & 1);
     const size_t rb_words = (size_t)GW * 16 * (K >> 3) - (size_t)16 * T;
-    const size_t rb_steps = (size_t)GW * 16 * ngroups - (size_t)4 * T;
-    const size_t rowB_steps = (size_t)8 * ngroups;
+    const size_t rb_steps = (size_t)GW * 16 * sstride;
+    const size_t rowB_steps = (size_t)8 * sstride;
     int lkt = 0;
     auto load = [&](int u) {
         wa[u] = ldg_stream_v4(lp);
         wb[u] = ldg_stream_v4(lp + K);
-        sa[u] = ldg_nc_u32(ls);
-        sb[u] = ldg_nc_u32(ls + rowB_steps);
+        sa[u] = step_pair<G32>(ls, lj, lg);
+        sb[u] = step_pair<G32>(ls + rowB_steps, lj, lg);
         lp += 16;
-        ls += 4;
+        lj += 4;
         if (++lkt == T) {
             lkt = 0;
             lp += rb_words;
             ls += rb_steps;
+            lj = 2 * (t & 1);
         }
     };
 
@@ -436,7 +464,7 @@ template <int U, bool ARGMAX>
 __global__ void __launch_bounds__(512)
 gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
-               int M, int N, int K, int ksplit, unsigned long long *__restrict__ keys)
+               int M, int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -455,16 +483,16 @@ gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     const int rA = min(rowA, N - 1), rB = min(rowB, N - 1);
     const uint32_t *qA = qw + (size_t)rA * (K >> 3) + t;
     const uint32_t *qB = qw + (size_t)rB * (K >> 3) + t;
-    const uint16_t *sA = sc + (size_t)rA * ngroups;
-    const uint16_t *sB = sc + (size_t)rB * ngroups;
+    const uint16_t *sA = sc + (size_t)rA * (ngroups >> lg);
+    const uint16_t *sB = sc + (size_t)rB * (ngroups >> lg);
 
     uint32_t wa[U], wb[U], sa[U], sb[U];
     auto load = [&](int u, int G) {
         if (active) {
             wa[u] = ldg_stream_u32(qA + 4 * G);
             wb[u] = ldg_stream_u32(qB + 4 * G);
-            sa[u] = ldg_nc_u16(sA + G);
-            sb[u] = ldg_nc_u16(sB + G);
+            sa[u] = ldg_nc_u16(sA + (G >> lg));
+            sb[u] = ldg_nc_u16(sB + (G >> lg));
         } else {
             wa[u] = wb[u] = 0x88888888u;
             sa[u] = sb[u] = 0u;
@@ -576,7 +604,7 @@ template <int U, bool ARGMAX>
 __global__ void __launch_bounds__(512)
 gemv_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
-               int M, int N, int K, int ksplit, unsigned long long *__restrict__ keys)
+               int M, int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -599,16 +627,28 @@ gemv_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     // gives lane t word t of each of the four groups, as the mma wants.
     const uint32_t *qA = qw + (size_t)rA * (K >> 3) + 4 * t;
     const uint32_t *qB = qw + (size_t)rB * (K >> 3) + 4 * t;
-    const uint16_t *sA = sc + (size_t)rA * ngroups;
-    const uint16_t *sB = sc + (size_t)rB * ngroups;
+    const uint16_t *sA = sc + (size_t)rA * (ngroups >> lg);
+    const uint16_t *sB = sc + (size_t)rB * (ngroups >> lg);
 
     uint4 wa[U], wb[U];
     uint2 sa[U], sb[U];
+    // The steps of the quad's four 32-code groups 4Q .. 4Q+3 as bf16 pairs
+    // (one step per 32 << lg codes).
+    auto steps4 = [&](const uint16_t *srow, int Q) -> uint2 {
+        if (lg == 0)
+            return ldg_nc_u64(srow + 4 * Q);
+        if (lg == 1) {
+            const uint32_t v = ldg_nc_u32(srow + 2 * Q);
+            return make_uint2((v & 0xFFFFu) | (v << 16), (v >> 16) | (v & 0xFFFF0000u));
+        }
+        const uint32_t v = ldg_nc_u16(srow + ((4 * Q) >> lg));
+        return make_uint2(v | (v << 16), v | (v << 16));
+    };
     auto load = [&](int u, int Q) {
         wa[u] = ldg_stream_v4(qA + 16 * Q);
         wb[u] = ldg_stream_v4(qB + 16 * Q);
-        sa[u] = ldg_nc_u64(sA + 4 * Q);
-        sb[u] = ldg_nc_u64(sB + 4 * Q);
+        sa[u] = steps4(sA, Q);
+        sb[u] = steps4(sB, Q);
     };
 
     if (threadIdx.x == 32)
@@ -874,7 +914,7 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
 
 template <int MX, bool ARGMAX>
 static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
-                             const uint16_t *sc, int N, int K, unsigned long long *keys,
+                             const uint16_t *sc, int N, int K, unsigned long long *keys, int lg,
                              cudaStream_t s)
 {
     const int Kpad = (K + kTileK - 1) / kTileK * kTileK;
@@ -883,21 +923,27 @@ static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, c
     if (p.ksplit > 1)
         smem += (size_t)rbc * p.ksplit * MX * 16 * sizeof(float);
     const bool sc32 = (K % 64) == 0, full = (K % kTileK) == 0;
-    auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, false, ARGMAX> : gemv_m2_kernel<MX, 4, false, false, ARGMAX>;
+    // Groups above 32 take the same kernels with a run-time step shift.
+    auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, false, ARGMAX, true> : gemv_m2_kernel<MX, 4, false, false, ARGMAX, true>;
     if (p.unroll == 8)
-        kern = sc32 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX> : gemv_m2_kernel<MX, 8, false, false, ARGMAX>;
+        kern = sc32 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX, true> : gemv_m2_kernel<MX, 8, false, false, ARGMAX, true>;
     if (full)
-        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX> : gemv_m2_kernel<MX, 4, true, true, ARGMAX>;
+        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX, true> : gemv_m2_kernel<MX, 4, true, true, ARGMAX, true>;
+    if (lg > 0) { // K % 64 == 0 here
+        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX, false> : gemv_m2_kernel<MX, 4, true, false, ARGMAX, false>;
+        if (full)
+            kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX, false> : gemv_m2_kernel<MX, 4, true, true, ARGMAX, false>;
+    }
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(kern, dim3(p.grid), dim3(32 * p.warps), smem, s, y, x, qw, sc, N, K, p.ksplit,
-                      keys);
+                      keys, lg);
 }
 
 template <bool ARGMAX>
 static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
-                             const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
+                             const uint16_t *sc, int M, int N, int K, unsigned long long *keys, int lg,
                              cudaStream_t s)
 {
     const int rbc = p.warps / p.ksplit;
@@ -913,7 +959,7 @@ static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, c
     if (e != cudaSuccess)
         return e;
     return launch_pdl(kern, dim3(p.grid), dim3(32 * p.warps), smem, s, y, x, qw, sc, M, N, K,
-                      p.ksplit, keys);
+                      p.ksplit, keys, lg);
 }
 
 size_t decode_smem_bytes(const DecodePlan &p, int M, int K)
@@ -929,39 +975,40 @@ size_t decode_smem_bytes(const DecodePlan &p, int M, int K)
 
 template <int MX, bool ARGMAX>
 static cudaError_t launch_persist(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
-                                  const uint16_t *sc, int N, int K, unsigned long long *keys, cudaStream_t s)
+                                  const uint16_t *sc, int N, int K, unsigned long long *keys, int lg,
+                                  cudaStream_t s)
 {
     const size_t smem = (size_t)MX * K * 2 + 16;
-    auto kern = gemv_m2_persist_kernel<MX, 4, 2, ARGMAX>;
+    auto kern = lg == 0 ? gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, true> : gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, false>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(kern, dim3(p.grid), dim3(256), smem, s, y, x, qw, sc, N, K, keys);
+    return launch_pdl(kern, dim3(p.grid), dim3(256), smem, s, y, x, qw, sc, N, K, keys, lg);
 }
 
 cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
-                       const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
+                       const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
                        int32_t *argmax, cudaStream_t s)
 {
     const bool am = argmax != nullptr;
     cudaError_t e;
     if (p.kernel == 3) {
         if (M == 1)
-            e = am ? launch_persist<1, true>(p, y, x, qw, sc, N, K, keys, s)
-                   : launch_persist<1, false>(p, y, x, qw, sc, N, K, keys, s);
+            e = am ? launch_persist<1, true>(p, y, x, qw, sc, N, K, keys, lg, s)
+                   : launch_persist<1, false>(p, y, x, qw, sc, N, K, keys, lg, s);
         else
-            e = am ? launch_persist<2, true>(p, y, x, qw, sc, N, K, keys, s)
-                   : launch_persist<2, false>(p, y, x, qw, sc, N, K, keys, s);
+            e = am ? launch_persist<2, true>(p, y, x, qw, sc, N, K, keys, lg, s)
+                   : launch_persist<2, false>(p, y, x, qw, sc, N, K, keys, lg, s);
     } else if (p.kernel == 2) {
         if (M == 1)
-            e = am ? launch_m2<1, true>(p, y, x, qw, sc, N, K, keys, s)
-                   : launch_m2<1, false>(p, y, x, qw, sc, N, K, keys, s);
+            e = am ? launch_m2<1, true>(p, y, x, qw, sc, N, K, keys, lg, s)
+                   : launch_m2<1, false>(p, y, x, qw, sc, N, K, keys, lg, s);
         else
-            e = am ? launch_m2<2, true>(p, y, x, qw, sc, N, K, keys, s)
-                   : launch_m2<2, false>(p, y, x, qw, sc, N, K, keys, s);
+            e = am ? launch_m2<2, true>(p, y, x, qw, sc, N, K, keys, lg, s)
+                   : launch_m2<2, false>(p, y, x, qw, sc, N, K, keys, lg, s);
     } else {
-        e = am ? launch_m8<true>(p, y, x, qw, sc, M, N, K, keys, s)
-               : launch_m8<false>(p, y, x, qw, sc, M, N, K, keys, s);
+        e = am ? launch_m8<true>(p, y, x, qw, sc, M, N, K, keys, lg, s)
+               : launch_m8<false>(p, y, x, qw, sc, M, N, K, keys, lg, s);
     }
     if (e != cudaSuccess || !am)
         return e;

@@ -7,6 +7,15 @@
 
 namespace w4 {
 
+// log2(group / 32) for the served group sizes 32, 64, 128, 256, 512; -1 otherwise.
+inline int group_shift(int group)
+{
+    for (int lg = 0; lg <= 4; ++lg)
+        if (group == (32 << lg))
+            return lg;
+    return -1;
+}
+
 // Per-shape launch plan of the decode kernels (M <= 8).
 struct DecodePlan {
     int kernel = 2; // 2: M <= 2 kernel (full-group 128-bit loads), 3: its persistent form for
@@ -23,8 +32,9 @@ size_t decode_smem_bytes(const DecodePlan &p, int M, int K);
 
 // Launches the decode kernel (and, when argmax != nullptr, the argmax pass that
 // reduces keys[M][plan.grid]).
+// lg: log2(group / 32); scales hold one step per 32 << lg codes ([N][K >> (5 + lg)]).
 cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
-                       const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
+                       const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
                        int32_t *argmax, cudaStream_t s);
 
 // Bulk-copy streaming decode kernel (M <= 2, K % 256 == 0, 16-byte aligned
@@ -49,7 +59,7 @@ cudaError_t run_argmax_finalize(int32_t *argmax, const unsigned long long *keys,
                                 cudaStream_t s);
 
 cudaError_t run_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qt,
-                             const uint16_t *sc, int M, int N, int K, int32_t *status,
+                             const uint16_t *sc, int M, int N, int K, int lg, int32_t *status,
                              cudaStream_t s);
 
 cudaError_t run_read_probe(unsigned long long *sum, const void *buf, size_t bytes, int num_sms,
@@ -69,7 +79,7 @@ struct PrefillPlan {
 
 PrefillPlan plan_prefill(int M, int N, int K, int num_sms, size_t ws_floats);
 cudaError_t run_prefill(const PrefillPlan &p, float *y, const uint16_t *x, const uint32_t *qw,
-                        const uint16_t *sc, int M, int N, int K, float *ws, int *err, cudaStream_t s);
+                        const uint16_t *sc, int M, int N, int K, int lg, float *ws, int *err, cudaStream_t s);
 
 // Decode attention of one query token (H <= 8 query heads sharing one key/value
 // head, D in {128, 256, 384, 512}) over T cache slots; split partials in ws.

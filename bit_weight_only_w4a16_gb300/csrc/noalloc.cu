@@ -89,7 +89,8 @@ extern "C" int w4a16_gemv_argmax_noalloc(float *y, int32_t *argmax, const uint16
         return W4_ERR_INVALID_ARG;
     if (M <= 0 || N <= 0 || K <= 0)
         return W4_ERR_INVALID_ARG;
-    if (group != 32)
+    const int lg = w4::group_shift(group);
+    if (lg < 0)
         return W4_ERR_UNSUPPORTED;
     if (K % group != 0)
         return W4_ERR_INVALID_ARG;
@@ -111,7 +112,7 @@ extern "C" int w4a16_gemv_argmax_noalloc(float *y, int32_t *argmax, const uint16
         return W4_ERR_UNSUPPORTED;
     if (w4::decode_smem_bytes(p, M, K) > 220 * 1024)
         return W4_ERR_UNSUPPORTED;
-    const cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, d->keys, argmax,
+    const cudaError_t e = w4::run_decode(p, y, x, qweight, scales, M, N, K, lg, d->keys, argmax,
                                          static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         cudaGetLastError();

@@ -23,7 +23,10 @@
  *   - Results are bitwise deterministic run to run (no floating-point atomics).
  *   - All calls are safe to capture in a CUDA graph once the library has been
  *     initialised on the device (w4_init, or any earlier call on that device).
- *   - group must be 32 (the only group size the pages use for this format).
+ *   - group is 32, 64, 128, 256 or 512 codes per step along K (32 is the
+ *     checkpoint paragraph's format; the "fastgemma-gemma-4-E2B" model card's
+ *     file table stores FFN and LM-head weights with group 256, the per-layer
+ *     table with group 64, and mentions a group-512 build); K % group == 0.
  *   - K must be a positive multiple of 32; N and M positive; N*K/8 and M*K must
  *     fit in int32 index space as stated per call.
  *   - Pointers must be 16-byte aligned (128-bit loads); y must be 4-byte aligned.
@@ -41,7 +44,7 @@ extern "C" {
 typedef enum {
     W4_OK = 0,
     W4_ERR_INVALID_ARG = 1,  /* NULL pointer, size <= 0, K % group != 0, size overflow */
-    W4_ERR_UNSUPPORTED = 2,  /* group != 32, M beyond what the call serves */
+    W4_ERR_UNSUPPORTED = 2,  /* group not in {32, 64, 128, 256, 512}, M beyond what the call serves */
     W4_ERR_MISALIGNED = 3,   /* a pointer is not aligned as stated above */
     W4_ERR_CUDA = 4,         /* the CUDA runtime reported an error (launch or allocation) */
     W4_ERR_NO_DEVICE = 5     /* no usable sm_103 device is current */

@@ -60,8 +60,13 @@ def test_validation_before_any_launch(lib):
     assert l.w4a16_gemv(A, A, A, A, 0, 16, 64, 32, None) == 1
     assert l.w4a16_gemv(A, A, A, A, 1, -1, 64, 32, None) == 1
     assert l.w4a16_gemv(A, A, A, A, 1, 16, 48, 32, None) == 1
-    # group other than 32
-    assert l.w4a16_gemv(A, A, A, A, 1, 16, 128, 64, None) == 2
+    # group outside {32, 64, 128, 256, 512}
+    assert l.w4a16_gemv(A, A, A, A, 1, 16, 96, 48, None) == 2
+    assert l.w4a16_gemv(A, A, A, A, 1, 16, 1024, 1024, None) == 2
+    assert l.w4a16_gemv(A, A, A, A, 1, 16, 64, 16, None) == 2
+    assert l.w4_embed_gather(A, A, A, A, 1, 10, 96, 48, None, None) == 2
+    # K not a multiple of a served group
+    assert l.w4a16_gemv(A, A, A, A, 1, 16, 96, 64, None) == 1
     # M beyond the decode call
     assert l.w4a16_gemv(A, A, A, A, 9, 16, 64, 32, None) == 2
     assert l.w4a16_gemv_argmax(A, A, A, A, A, 9, 16, 64, 32, None) == 2

@@ -237,3 +237,26 @@ def test_size_arithmetic_matches_the_pages():
     assert 262144 * 1536 * 2 == int(0.75 * 2 ** 30)
     # 1,222.8 MiB read in 9.12 ms is 140.6 GB/s.
     assert abs(1222.8 * 2 ** 20 / 9.12e-3 / 1e9 - 140.6) < 0.05
+
+
+@pytest.mark.parametrize("group", [64, 128, 256, 512])
+def test_group_equals_repeated_group32_steps(group):
+    """A group-G step applies to G consecutive codes: the same problem written
+    with group 32 and each step repeated G/32 times gives bit-identical y, |y|
+    sums, dequantized weights and gathered rows (a wrong step index or row
+    stride for G != 32 breaks this)."""
+    M, N, K = 3, 5, 1024
+    x = synth.gen_x(900 + group, M, K)
+    qw = synth.gen_qweight(900 + group, N, K)
+    scg = synth.gen_scales(900 + group, N, K, group)
+    sc32 = np.repeat(scg, group // 32, axis=1)
+    assert sc32.shape == (N, K // 32)
+    y1, a1 = oracle.gemm(x, qw, scg, group)
+    y2, a2 = oracle.gemm(x, qw, sc32, 32)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(a1, a2)
+    np.testing.assert_array_equal(oracle.dequant(qw, scg, group), oracle.dequant(qw, sc32, 32))
+    ids = np.array([4, 0, 2], dtype=np.int32)
+    g1, _ = oracle.embed_gather(ids, qw, scg, group)
+    g2, _ = oracle.embed_gather(ids, qw, sc32, 32)
+    np.testing.assert_array_equal(g1, g2)
