@@ -191,11 +191,7 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint4 b = xb[xi * i];
-            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
-            unpack_word(a_w[i], a04, a15, a26, a37);
-            unpack_word(b_w[i], b04, b15, b26, b37);
-            mma_16816(c, a04, b04, a15, b15, b.x, b.y);
-            mma_16816(d, a26, b26, a37, b37, b.z, b.w);
+            unpack_mma2(c, d, a_w[i], b_w[i], b.x, b.y, b.z, b.w);
         }
         accA = fmaf(bf16lo_to_f32(sa[u]), c[0] + d[0], accA);
         accA = fmaf(bf16hi_to_f32(sa[u]), c[1] + d[1], accA);
@@ -365,18 +361,8 @@ gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint4 b0 = xb[xi * i], b1 = xb[xstep + xi * i];
-            const uint32_t wa0 = (&wa[u].x)[i], wb0 = (&wb[u].x)[i];
-            const uint32_t wa1 = (&wa[u + 1].x)[i], wb1 = (&wb[u + 1].x)[i];
-            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
-            uint32_t e04, e15, e26, e37, f04, f15, f26, f37;
-            unpack_word(wa0, a04, a15, a26, a37);
-            unpack_word(wb0, b04, b15, b26, b37);
-            unpack_word(wa1, e04, e15, e26, e37);
-            unpack_word(wb1, f04, f15, f26, f37);
-            mma_16816(c0, a04, b04, a15, b15, b0.x, b0.y);
-            mma_16816(c1, e04, f04, e15, f15, b1.x, b1.y);
-            mma_16816(d0, a26, b26, a37, b37, b0.z, b0.w);
-            mma_16816(d1, e26, f26, e37, f37, b1.z, b1.w);
+            unpack_mma2(c0, d0, (&wa[u].x)[i], (&wb[u].x)[i], b0.x, b0.y, b0.z, b0.w);
+            unpack_mma2(c1, d1, (&wa[u + 1].x)[i], (&wb[u + 1].x)[i], b1.x, b1.y, b1.z, b1.w);
         }
         accA = fmaf(bf16lo_to_f32(sa[u]), c0[0] + d0[0], accA);
         accA = fmaf(bf16hi_to_f32(sa[u]), c0[1] + d0[1], accA);
