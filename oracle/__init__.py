@@ -44,6 +44,10 @@ def _load():
         lib.w4o_embed_gather.restype = None
         lib.w4o_sum_words.argtypes = [P, I]
         lib.w4o_sum_words.restype = ctypes.c_uint64
+        lib.w4o_hadamard_rows.argtypes = [P, P, I, I, I]
+        lib.w4o_hadamard_rows.restype = None
+        lib.w4o_gemm_rows_xf64.argtypes = [P, P, P, P, P, I, I, I, I, P, I]
+        lib.w4o_gemm_rows_xf64.restype = None
         lib.w4o_attn_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, ctypes.c_double, P]
         lib.w4o_attn_decode.restype = None
         lib.w4o_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -155,3 +159,37 @@ def attn_decode(q, k, v, kpos=None, qpos=None, window: int = 0, scale: float = 1
     lib.w4o_attn_decode(_ptr(out), _ptr(absout), _ptr(q), _ptr(k), _ptr(v),
                         None if kp is None else _ptr(kp), qp, int(window), H, T, D, float(scale), _ptr(s))
     return out, absout
+
+
+def hadamard(x, b: int):
+    """fp64 [M][K]: x (bf16 bits) times blockdiag(H_b) with H_b[i][j] = (-1)^popcount(i&j)/sqrt(b)."""
+    lib = _load()
+    x = _c(np.atleast_2d(x), np.uint16)
+    M, K = x.shape
+    assert b >= 1 and (b & (b - 1)) == 0 and K % b == 0
+    out = np.empty((M, K), dtype=np.float64)
+    lib.w4o_hadamard_rows(_ptr(out), _ptr(x), M, K, b)
+    return out
+
+
+def gemm_xf64(x, qweight, scales, group: int = 32, rows=None):
+    """gemm() with an fp64 activation [M][K] (e.g. hadamard(x, b))."""
+    lib = _load()
+    x = _c(np.atleast_2d(x), np.float64)
+    qweight = _c(qweight, np.uint32)
+    scales = _c(scales, np.uint16)
+    M, K = x.shape
+    N = qweight.shape[0]
+    assert qweight.shape[1] * 8 == K and scales.shape == (N, K // group)
+    r = None if rows is None else _c(rows, np.int64)
+    nr = N if r is None else r.shape[0]
+    y = np.empty((M, nr), dtype=np.float64)
+    a = np.empty((M, nr), dtype=np.float64)
+    lib.w4o_gemm_rows_xf64(_ptr(y), _ptr(a), _ptr(x), _ptr(qweight), _ptr(scales), M, N, K, group,
+                           None if r is None else _ptr(r), nr)
+    return y, a
+
+
+def gemm_hadamard(x, qweight, scales, hblock: int, group: int = 32, rows=None):
+    """(y, absy): the rotated product (x H) W'^T with W' = dequant(qweight, scales)."""
+    return gemm_xf64(hadamard(x, hblock), qweight, scales, group, rows)

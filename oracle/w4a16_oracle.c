@@ -35,6 +35,12 @@
  *   R3  The gather output is bf16, round-to-nearest-even of the exact product.
  *   R4  Argmax is the lowest index of the largest value; -0 equals +0.
  *   R5  The read probe's result is the sum of all 32-bit words mod 2^64.
+ *   R7  Hadamard rotation ("fastgemma-gemma-4-E2B" card: every linear weight is
+ *       rotated along K, W' = W H^T, and a runtime fast Walsh-Hadamard
+ *       transform of the activation makes the product identical): H is
+ *       block-diagonal over blocks of b consecutive k, each block the Sylvester
+ *       matrix H_b[i][j] = (-1)^popcount(i & j) / sqrt(b), which is symmetric and
+ *       orthogonal; the rotated product is y = (x H) W'^T.
  *   R6  Attention scores are scale * (q . k) with the scale an argument (the
  *       pages' listing multiplies q by k^T and names no scale); a query with no
  *       kept slot gives a zero output.
@@ -242,6 +248,50 @@ void w4o_attn_decode(double *out, double *absout, const uint16_t *q, const uint1
                 out[h * D + d] += w * vv;
                 absout[h * D + d] += w * fabs(vv);
             }
+        }
+    }
+}
+
+/*
+ * R7: xr[m][k] = sum_j x[m][j] * H_b[j mod b][k mod b] over the block of k, in
+ * fp64, by the definition (no butterflies): b must be a power of two dividing K.
+ */
+void w4o_hadamard_rows(double *xr, const uint16_t *x, int64_t M, int64_t K, int64_t b)
+{
+    const double norm = 1.0 / sqrt((double)b);
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k = 0; k < K; ++k) {
+            const int64_t blk = k - k % b, kk = k % b;
+            double acc = 0.0;
+            for (int64_t j = 0; j < b; ++j) {
+                const int sign = __builtin_popcountll((unsigned long long)(j & kk)) & 1;
+                const double v = bf16_to_double(x[m * K + blk + j]);
+                acc += sign ? -v : v;
+            }
+            xr[m * K + k] = acc * norm;
+        }
+    }
+}
+
+/* w4o_gemm_rows with an fp64 activation (the rotated x of R7). */
+void w4o_gemm_rows_xf64(double *y, double *absy,
+                        const double *x, const uint32_t *qweight, const uint16_t *scales,
+                        int64_t M, int64_t N, int64_t K, int64_t group,
+                        const int64_t *rows, int64_t nrows)
+{
+    (void)N;
+    for (int64_t j = 0; j < nrows; ++j) {
+        int64_t n = rows ? rows[j] : j;
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0, acc_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double t = x[m * K + k] * weight_at(qweight, scales, K, group, n, k);
+                acc += t;
+                acc_abs += fabs(t);
+            }
+            y[m * nrows + j] = acc;
+            if (absy)
+                absy[m * nrows + j] = acc_abs;
         }
     }
 }
