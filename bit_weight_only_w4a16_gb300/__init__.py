@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED",
 # Symbols declared in include/w4a16.h.
 EXPORTS = ("w4_status_string", "w4_last_cuda_error", "w4_init", "w4_device_error", "w4a16_gemv", "w4a16_gemm",
            "w4a16_gemv_argmax", "w4a16_gemv_argmax_noalloc", "w4_embed_gather", "hbm_read_probe",
-           "w4_attn_decode")
+           "w4_attn_decode", "w4a16_gemv_hadamard")
 
 
 class W4Error(RuntimeError):
@@ -63,6 +63,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hbm_read_probe.restype = I
     lib.w4_attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, ctypes.c_float, P]
     lib.w4_attn_decode.restype = I
+    lib.w4a16_gemv_hadamard.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
+    lib.w4a16_gemv_hadamard.restype = I
     return lib
 
 
@@ -216,3 +218,20 @@ def w4_attn_decode(q, k, v, kpos=None, qpos=None, window: int = 0, scale: float 
     _check(_lib.w4_attn_decode(_ptr(o), _ptr(q), _ptr(k), _ptr(v), _ptr(kpos), qp, int(window), H, T, D,
                                float(scale), _stream(stream)), "w4_attn_decode")
     return o
+
+
+def w4a16_gemv_hadamard(x, qweight, scales, hblock: int, group: int = 32, out=None, argmax=False,
+                        stream=None):
+    """y fp32 [M][N] = (x H) W'^T for Hadamard-rotated weights W' (M <= 4); with
+    argmax=True (or an int32 [M] tensor) also the lowest index of each row's max."""
+    _bits16(x, "x"); _u32(qweight, "qweight"); _bits16(scales, "scales")
+    M, N, K = _shape(x, qweight, scales, group)
+    y = torch.empty((M, N), dtype=torch.float32, device=x.device) if out is None else _cuda(out, "out")
+    a = None
+    if argmax is True:
+        a = torch.empty((M,), dtype=torch.int32, device=x.device)
+    elif argmax is not False and argmax is not None:
+        a = _cuda(argmax, "argmax")
+    _check(_lib.w4a16_gemv_hadamard(_ptr(y), _ptr(a), _ptr(x), _ptr(qweight), _ptr(scales), M, N, K, group,
+                                    int(hblock), _stream(stream)), "w4a16_gemv_hadamard")
+    return (y, a) if a is not None else y

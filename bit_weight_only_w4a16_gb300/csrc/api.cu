@@ -330,4 +330,36 @@ int w4_attn_decode(float *out, const uint16_t *q, const uint16_t *k, const uint1
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 
+int w4a16_gemv_hadamard(float *y, int32_t *argmax, const uint16_t *x, const uint32_t *qweight,
+                        const uint16_t *scales, int M, int N, int K, int group, int hblock, void *stream)
+{
+    int rc = check_w4_args(y, x, qweight, scales, M, N, K, group);
+    if (rc != W4_OK)
+        return rc;
+    if (hblock < 2 || hblock > 4096 || (hblock & (hblock - 1)) != 0)
+        return W4_ERR_UNSUPPORTED;
+    if (K % hblock != 0)
+        return W4_ERR_INVALID_ARG;
+    if (M > 4)
+        return W4_ERR_UNSUPPORTED;
+    if (argmax && !aligned(argmax, 4))
+        return W4_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    if ((rc = device_state(&st)) != W4_OK)
+        return rc;
+    // The rotated activation's (hi, lo) rows live in the split scratch.
+    if ((size_t)2 * M * K * sizeof(uint16_t) > kWsFloats * sizeof(float))
+        return W4_ERR_UNSUPPORTED;
+    const w4::DecodePlan p = w4::plan_decode(2 * M, N, K, st->num_sms);
+    if (!decode_fits(p, 2 * M, K) || (argmax && (size_t)M * p.grid > kKeyCapacity))
+        return W4_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint16_t *x2 = reinterpret_cast<uint16_t *>(st->ws);
+    cudaError_t e = w4::run_hadamard_split(x2, x, M, K, hblock, s);
+    if (e == cudaSuccess)
+        e = w4::run_decode(p, y, x2, qweight, scales, 2 * M, N, K, w4::group_shift(group),
+                           argmax ? st->keys : nullptr, argmax, s, true);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
 } // extern "C"

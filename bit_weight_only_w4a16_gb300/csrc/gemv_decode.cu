@@ -84,7 +84,9 @@ __device__ __forceinline__ uint32_t step_pair(const uint16_t *srow, int j, int l
 // FULL (K % 128 == 0, implies SC32): every k-tile is whole, so the loads need
 // no per-group guards; warps past the last row block load clamped rows and
 // never store.
-template <int MX, int U, bool SC32, bool FULL, bool ARGMAX, bool G32>
+// PAIRS: x rows come as (hi, lo) pairs of one activation row (the two bf16
+// parts of an fp32 value); each output row is the sum of its pair.
+template <int MX, int U, bool SC32, bool FULL, bool ARGMAX, bool G32, bool PAIRS>
 __global__ void __launch_bounds__(512)
 gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
@@ -213,12 +215,17 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     // Lanes t and t^1 hold the two group-slot pairs of the same (row, x-row).
     accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
     accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+    if (PAIRS) { // x-rows 0 (lanes t < 2) and 1 (t >= 2) are one output row
+        accA += __shfl_xor_sync(0xFFFFFFFFu, accA, 2);
+        accB += __shfl_xor_sync(0xFFFFFFFFu, accB, 2);
+    }
+    constexpr int MO = PAIRS ? MX / 2 : MX; // output rows
     const int m = t >> 1;
-    const bool writer = ((t & 1) == 0) && (m < MX);
+    const bool writer = ((t & 1) == 0) && (m < MO);
 
-    __shared__ unsigned long long ck[MX];
+    __shared__ unsigned long long ck[MO];
     if (ARGMAX) {
-        if (threadIdx.x < MX)
+        if (threadIdx.x < MO)
             ck[threadIdx.x] = 0ull;
         __syncthreads();
     }
@@ -238,19 +245,19 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         }
     } else {
         // Fixed-order reduction of the k-slices through shared memory.
-        float *red = reinterpret_cast<float *>(zero_chunk + 1); // [rbc][ksplit][MX][16]
+        float *red = reinterpret_cast<float *>(zero_chunk + 1); // [rbc][ksplit][MO][16]
         if (writer) {
-            float *r = red + ((rbl * ksplit + ks) * MX + m) * 16;
+            float *r = red + ((rbl * ksplit + ks) * MO + m) * 16;
             r[g] = accA;
             r[g + 8] = accB;
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < rbc * MX * 16; i += blockDim.x) {
-            const int rr = i & 15, mm = (i >> 4) % MX, rl = i / (16 * MX);
+        for (int i = threadIdx.x; i < rbc * MO * 16; i += blockDim.x) {
+            const int rr = i & 15, mm = (i >> 4) % MO, rl = i / (16 * MO);
             const int row = (blockIdx.x * rbc + rl) * 16 + rr;
             float s = 0.f;
             for (int k2 = 0; k2 < ksplit; ++k2)
-                s += red[((rl * ksplit + k2) * MX + mm) * 16 + rr];
+                s += red[((rl * ksplit + k2) * MO + mm) * 16 + rr];
             if (row < N) {
                 y[(size_t)mm * N + row] = s;
                 if (ARGMAX)
@@ -261,7 +268,7 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 
     if (ARGMAX) {
         __syncthreads();
-        if (threadIdx.x < MX)
+        if (threadIdx.x < MO)
             keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
     }
 }
@@ -277,7 +284,7 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 // 59.0 -> 48.9 us for a 262144 x 1536 GEMV against one tile at a time with
 // addresses recomputed per load; 4 tiles in flight per warp (105 registers)
 // then beat 6, 8 or 12 (46.3 vs 48.1, 49.0, 63.0 us) and 3 or 4 CTAs per SM.
-template <int MX, int U, int MINB, bool ARGMAX, bool G32>
+template <int MX, int U, int MINB, bool ARGMAX, bool G32, bool PAIRS>
 __global__ void __launch_bounds__(256, MINB)
 gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                        const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc, int N, int K,
@@ -335,10 +342,11 @@ gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     const int chunks_per_row = K >> 3;
     stage_x_rows(xs, x, MX, K, chunks_per_row);
     uint4 *zero_chunk = xs + MX * chunks_per_row;
-    __shared__ unsigned long long ck[MX];
+    constexpr int MO = PAIRS ? MX / 2 : MX; // output rows (PAIRS: x-rows 0, 1 are one)
+    __shared__ unsigned long long ck[MO];
     if (threadIdx.x == 0)
         *zero_chunk = make_uint4(0u, 0u, 0u, 0u);
-    if (ARGMAX && threadIdx.x < MX)
+    if (ARGMAX && threadIdx.x < MO)
         ck[threadIdx.x] = 0ull;
     __syncthreads();
 
@@ -348,7 +356,7 @@ gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     const int xstep = bsel ? 16 : 0;
     const int xi = bsel ? 1 : 0;
     const int m = t >> 1;
-    const bool writer = ((t & 1) == 0) && (m < MX);
+    const bool writer = ((t & 1) == 0) && (m < MO);
 
     float accA = 0.f, accB = 0.f;
     int cj = 0, ckt = 0; // compute cursor
@@ -374,8 +382,12 @@ gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         accB = fmaf(bf16hi_to_f32(sb[u + 1]), c1[3] + d1[3], accB);
     };
     auto finish = [&]() {
-        const float a = accA + __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
-        const float b = accB + __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+        float a = accA + __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
+        float b = accB + __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+        if (PAIRS) {
+            a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+            b += __shfl_xor_sync(0xFFFFFFFFu, b, 2);
+        }
         const int rowA = (gw + cj * GW) * 16 + g, rowB = rowA + 8;
         if (writer) {
             if (rowA < N) {
@@ -414,7 +426,7 @@ gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 
     if (ARGMAX) {
         __syncthreads();
-        if (threadIdx.x < MX)
+        if (threadIdx.x < MO)
             keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
     }
 }
@@ -446,7 +458,77 @@ __device__ __forceinline__ void quad_transpose4(uint32_t (&v)[4], int t)
     }
 }
 
-template <int U, bool ARGMAX>
+// Output of the M <= 8 kernels: lane (g, t) holds y[2t][rowA], y[2t+1][rowA],
+// y[2t][rowB], y[2t+1][rowB] of its warp's K slice; with ksplit > 1 the slices
+// are added in fixed order through shared memory (red: [rbc][ksplit][8][16]).
+// PAIRS: x-rows 2t and 2t+1 are the two parts of output row t (M/2 outputs).
+// CTA-best argmax key per output row; max is order-independent (deterministic).
+template <bool ARGMAX, bool PAIRS>
+__device__ __forceinline__ void m8_store(float *__restrict__ y, float a0, float a1, float b0, float b1,
+                                         int M, int N, int g, int t, int rowA, int rowB, bool active,
+                                         int ksplit, int ks, int rbl, int rbc, float *red,
+                                         unsigned long long *__restrict__ keys)
+{
+    __shared__ unsigned long long ck[8];
+    if (ARGMAX) {
+        if (threadIdx.x < 8)
+            ck[threadIdx.x] = 0ull;
+        __syncthreads();
+    }
+    if (PAIRS) {
+        a0 += a1;
+        b0 += b1;
+    }
+    const int Mout = PAIRS ? M / 2 : M;
+    const int m0 = PAIRS ? t : 2 * t, m1 = 2 * t + 1;
+    constexpr int NJ = PAIRS ? 1 : 2;
+    if (ksplit == 1) {
+        if (active) {
+            const float v[2][2] = {{a0, a1}, {b0, b1}};
+            const int rows[2] = {rowA, rowB};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int j = 0; j < NJ; ++j) {
+                    const int mm = j ? m1 : m0;
+                    if (rows[h] < N && mm < Mout) {
+                        y[(size_t)mm * N + rows[h]] = v[h][j];
+                        if (ARGMAX)
+                            atomicMax(&ck[mm], argmax_key(v[h][j], rows[h]));
+                    }
+                }
+            }
+        }
+    } else {
+        float *r = red + (rbl * ksplit + ks) * 8 * 16;
+        r[m0 * 16 + g] = a0;
+        r[m0 * 16 + g + 8] = b0;
+        if (!PAIRS) {
+            r[m1 * 16 + g] = a1;
+            r[m1 * 16 + g + 8] = b1;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < rbc * 8 * 16; i += blockDim.x) {
+            const int rr = i & 15, mm = (i >> 4) & 7, rl = i >> 7;
+            const int row = (blockIdx.x * rbc + rl) * 16 + rr;
+            if (row < N && mm < Mout) {
+                float sum = 0.f;
+                for (int k2 = 0; k2 < ksplit; ++k2)
+                    sum += red[((rl * ksplit + k2) * 8 + mm) * 16 + rr];
+                y[(size_t)mm * N + row] = sum;
+                if (ARGMAX)
+                    atomicMax(&ck[mm], argmax_key(sum, row));
+            }
+        }
+    }
+    if (ARGMAX) {
+        __syncthreads();
+        if (threadIdx.x < Mout)
+            keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
+    }
+}
+
+template <int U, bool ARGMAX, bool PAIRS>
 __global__ void __launch_bounds__(512)
 gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
@@ -532,61 +614,11 @@ gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         }
     }
 
-    // Lane (g, t) holds y[2t][rowA], y[2t+1][rowA], y[2t][rowB], y[2t+1][rowB].
-    // CTA-best argmax key per x-row; max is order-independent, so deterministic.
-    __shared__ unsigned long long ck[8];
-    if (ARGMAX) {
-        if (threadIdx.x < 8)
-            ck[threadIdx.x] = 0ull;
-        __syncthreads();
-    }
-    const int m0 = 2 * t, m1 = 2 * t + 1;
-    if (ksplit == 1) {
-        if (active) {
-            const float v[2][2] = {{a0, a1}, {b0, b1}};
-            const int rows[2] = {rowA, rowB};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int mm = j ? m1 : m0;
-                    if (rows[h] < N && mm < M) {
-                        y[(size_t)mm * N + rows[h]] = v[h][j];
-                        if (ARGMAX)
-                            atomicMax(&ck[mm], argmax_key(v[h][j], rows[h]));
-                    }
-                }
-            }
-        }
-    } else {
-        float *red = reinterpret_cast<float *>(xs + 8 * cpr); // [rbc][ksplit][8][16]
-        float *r = red + (rbl * ksplit + ks) * 8 * 16;
-        r[m0 * 16 + g] = a0;
-        r[m1 * 16 + g] = a1;
-        r[m0 * 16 + g + 8] = b0;
-        r[m1 * 16 + g + 8] = b1;
-        __syncthreads();
-        for (int i = threadIdx.x; i < rbc * 8 * 16; i += blockDim.x) {
-            const int rr = i & 15, mm = (i >> 4) & 7, rl = i >> 7;
-            const int row = (blockIdx.x * rbc + rl) * 16 + rr;
-            float s = 0.f;
-            for (int k2 = 0; k2 < ksplit; ++k2)
-                s += red[((rl * ksplit + k2) * 8 + mm) * 16 + rr];
-            if (row < N && mm < M) {
-                y[(size_t)mm * N + row] = s;
-                if (ARGMAX)
-                    atomicMax(&ck[mm], argmax_key(s, row));
-            }
-        }
-    }
-    if (ARGMAX) {
-        __syncthreads();
-        if (threadIdx.x < M)
-            keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
-    }
+    m8_store<ARGMAX, PAIRS>(y, a0, a1, b0, b1, M, N, g, t, rowA, rowB, active, ksplit, ks, rbl, rbc,
+                            reinterpret_cast<float *>(xs + 8 * cpr), keys);
 }
 
-template <int U, bool ARGMAX>
+template <int U, bool ARGMAX, bool PAIRS>
 __global__ void __launch_bounds__(512)
 gemv_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
@@ -694,58 +726,8 @@ gemv_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         }
     }
 
-    // Lane (g, t) holds y[2t][rowA], y[2t+1][rowA], y[2t][rowB], y[2t+1][rowB].
-    // CTA-best argmax key per x-row; max is order-independent, so deterministic.
-    __shared__ unsigned long long ck[8];
-    if (ARGMAX) {
-        if (threadIdx.x < 8)
-            ck[threadIdx.x] = 0ull;
-        __syncthreads();
-    }
-    const int m0 = 2 * t, m1 = 2 * t + 1;
-    if (ksplit == 1) {
-        if (active) {
-            const float v[2][2] = {{a0, a1}, {b0, b1}};
-            const int rows[2] = {rowA, rowB};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int mm = j ? m1 : m0;
-                    if (rows[h] < N && mm < M) {
-                        y[(size_t)mm * N + rows[h]] = v[h][j];
-                        if (ARGMAX)
-                            atomicMax(&ck[mm], argmax_key(v[h][j], rows[h]));
-                    }
-                }
-            }
-        }
-    } else {
-        float *red = reinterpret_cast<float *>(xs + 8 * cpr); // [rbc][ksplit][8][16]
-        float *r = red + (rbl * ksplit + ks) * 8 * 16;
-        r[m0 * 16 + g] = a0;
-        r[m1 * 16 + g] = a1;
-        r[m0 * 16 + g + 8] = b0;
-        r[m1 * 16 + g + 8] = b1;
-        __syncthreads();
-        for (int i = threadIdx.x; i < rbc * 8 * 16; i += blockDim.x) {
-            const int rr = i & 15, mm = (i >> 4) & 7, rl = i >> 7;
-            const int row = (blockIdx.x * rbc + rl) * 16 + rr;
-            float s = 0.f;
-            for (int k2 = 0; k2 < ksplit; ++k2)
-                s += red[((rl * ksplit + k2) * 8 + mm) * 16 + rr];
-            if (row < N && mm < M) {
-                y[(size_t)mm * N + row] = s;
-                if (ARGMAX)
-                    atomicMax(&ck[mm], argmax_key(s, row));
-            }
-        }
-    }
-    if (ARGMAX) {
-        __syncthreads();
-        if (threadIdx.x < M)
-            keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
-    }
+    m8_store<ARGMAX, PAIRS>(y, a0, a1, b0, b1, M, N, g, t, rowA, rowB, active, ksplit, ks, rbl, rbc,
+                            reinterpret_cast<float *>(xs + 8 * cpr), keys);
 }
 
 // ---------------------------------------------------- argmax finalize ----
@@ -898,7 +880,7 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
     return p;
 }
 
-template <int MX, bool ARGMAX>
+template <int MX, bool ARGMAX, bool PAIRS>
 static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                              const uint16_t *sc, int N, int K, unsigned long long *keys, int lg,
                              cudaStream_t s)
@@ -910,15 +892,20 @@ static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, c
         smem += (size_t)rbc * p.ksplit * MX * 16 * sizeof(float);
     const bool sc32 = (K % 64) == 0, full = (K % kTileK) == 0;
     // Groups above 32 take the same kernels with a run-time step shift.
-    auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, false, ARGMAX, true> : gemv_m2_kernel<MX, 4, false, false, ARGMAX, true>;
+    auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, false, ARGMAX, true, PAIRS>
+                     : gemv_m2_kernel<MX, 4, false, false, ARGMAX, true, PAIRS>;
     if (p.unroll == 8)
-        kern = sc32 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX, true> : gemv_m2_kernel<MX, 8, false, false, ARGMAX, true>;
+        kern = sc32 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX, true, PAIRS>
+                    : gemv_m2_kernel<MX, 8, false, false, ARGMAX, true, PAIRS>;
     if (full)
-        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX, true> : gemv_m2_kernel<MX, 4, true, true, ARGMAX, true>;
+        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX, true, PAIRS>
+                             : gemv_m2_kernel<MX, 4, true, true, ARGMAX, true, PAIRS>;
     if (lg > 0) { // K % 64 == 0 here
-        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX, false> : gemv_m2_kernel<MX, 4, true, false, ARGMAX, false>;
+        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX, false, PAIRS>
+                             : gemv_m2_kernel<MX, 4, true, false, ARGMAX, false, PAIRS>;
         if (full)
-            kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX, false> : gemv_m2_kernel<MX, 4, true, true, ARGMAX, false>;
+            kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX, false, PAIRS>
+                                 : gemv_m2_kernel<MX, 4, true, true, ARGMAX, false, PAIRS>;
     }
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
@@ -927,7 +914,7 @@ static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, c
                       keys, lg);
 }
 
-template <bool ARGMAX>
+template <bool ARGMAX, bool PAIRS>
 static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                              const uint16_t *sc, int M, int N, int K, unsigned long long *keys, int lg,
                              cudaStream_t s)
@@ -936,11 +923,11 @@ static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, c
     size_t smem = (size_t)8 * K * 2;
     if (p.ksplit > 1)
         smem += (size_t)rbc * p.ksplit * 8 * 16 * sizeof(float);
-    auto kern = gemv_m8_kernel<8, ARGMAX>;
+    auto kern = gemv_m8_kernel<8, ARGMAX, PAIRS>;
     // 128-bit code loads with a quad transpose when K % 128 == 0 and the steps
     // allow 8-byte loads.
     if (K % kTileK == 0 && (reinterpret_cast<uintptr_t>(sc) & 7) == 0)
-        kern = gemv_m8q_kernel<4, ARGMAX>;
+        kern = gemv_m8q_kernel<4, ARGMAX, PAIRS>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
@@ -959,46 +946,53 @@ size_t decode_smem_bytes(const DecodePlan &p, int M, int K)
     return (size_t)8 * K * 2 + (p.ksplit > 1 ? rbc * p.ksplit * 8 * 16 * sizeof(float) : 0);
 }
 
-template <int MX, bool ARGMAX>
+template <int MX, bool ARGMAX, bool PAIRS>
 static cudaError_t launch_persist(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                                   const uint16_t *sc, int N, int K, unsigned long long *keys, int lg,
                                   cudaStream_t s)
 {
     const size_t smem = (size_t)MX * K * 2 + 16;
-    auto kern = lg == 0 ? gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, true> : gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, false>;
+    auto kern = lg == 0 ? gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, true, PAIRS>
+                        : gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, false, PAIRS>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(kern, dim3(p.grid), dim3(256), smem, s, y, x, qw, sc, N, K, keys, lg);
 }
 
+template <bool PAIRS>
+static cudaError_t dispatch_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                                   const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
+                                   bool am, cudaStream_t s)
+{
+    if (p.kernel == 3) {
+        if (M == 1 && !PAIRS)
+            return am ? launch_persist<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, s)
+                      : launch_persist<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, s);
+        return am ? launch_persist<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, s)
+                  : launch_persist<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, s);
+    }
+    if (p.kernel == 2) {
+        if (M == 1 && !PAIRS)
+            return am ? launch_m2<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, s)
+                      : launch_m2<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, s);
+        return am ? launch_m2<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, s)
+                  : launch_m2<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, s);
+    }
+    return am ? launch_m8<true, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s)
+              : launch_m8<false, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s);
+}
+
 cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                        const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
-                       int32_t *argmax, cudaStream_t s)
+                       int32_t *argmax, cudaStream_t s, bool pairs)
 {
     const bool am = argmax != nullptr;
-    cudaError_t e;
-    if (p.kernel == 3) {
-        if (M == 1)
-            e = am ? launch_persist<1, true>(p, y, x, qw, sc, N, K, keys, lg, s)
-                   : launch_persist<1, false>(p, y, x, qw, sc, N, K, keys, lg, s);
-        else
-            e = am ? launch_persist<2, true>(p, y, x, qw, sc, N, K, keys, lg, s)
-                   : launch_persist<2, false>(p, y, x, qw, sc, N, K, keys, lg, s);
-    } else if (p.kernel == 2) {
-        if (M == 1)
-            e = am ? launch_m2<1, true>(p, y, x, qw, sc, N, K, keys, lg, s)
-                   : launch_m2<1, false>(p, y, x, qw, sc, N, K, keys, lg, s);
-        else
-            e = am ? launch_m2<2, true>(p, y, x, qw, sc, N, K, keys, lg, s)
-                   : launch_m2<2, false>(p, y, x, qw, sc, N, K, keys, lg, s);
-    } else {
-        e = am ? launch_m8<true>(p, y, x, qw, sc, M, N, K, keys, lg, s)
-               : launch_m8<false>(p, y, x, qw, sc, M, N, K, keys, lg, s);
-    }
+    cudaError_t e = pairs ? dispatch_decode<true>(p, y, x, qw, sc, M, N, K, lg, keys, am, s)
+                          : dispatch_decode<false>(p, y, x, qw, sc, M, N, K, lg, keys, am, s);
     if (e != cudaSuccess || !am)
         return e;
-    return run_argmax_finalize(argmax, keys, M, p.grid, s);
+    return run_argmax_finalize(argmax, keys, pairs ? M / 2 : M, p.grid, s);
 }
 
 cudaError_t run_argmax_finalize(int32_t *argmax, const unsigned long long *keys, int M, int nblocks,

@@ -1,0 +1,84 @@
+// Walsh-Hadamard transform of the activation for Hadamard-rotated W4 weights.
+//
+// Source: "fastgemma-gemma-4-E2B" model card, "What is in the file": every
+// linear weight is Hadamard-rotated along K (W' = W H^T, H orthogonal), and a
+// runtime fast Walsh-Hadamard transform of the activation makes the product
+// identical while both weight groups and activation rows lose their outliers.
+// H = blockdiag(H_b) over blocks of b consecutive k, H_b[i][j] =
+// (-1)^popcount(i & j) / sqrt(b) (symmetric), so y = x W^T = (x H) W'^T.
+//
+// GB300 design. x H is computed once per call, in fp32, by one CTA per (x-row,
+// block of b): the log2(b) butterfly stages run in shared memory and the result
+// is split into two bf16 parts, hi = bf16(v) and lo = bf16(v - hi), so that
+// |v - hi - lo| <= 2^-18 |v| (a single bf16 would cost 2^-9, far above the
+// decode tolerance). The parts are written as x-rows 2m and 2m+1 of a scratch
+// activation; the decode kernels run on the 2M rows and add each pair before
+// storing. For M = 1 the pair fills the mma columns that a single row leaves
+// empty, so the split costs no tensor work and no extra weight traffic.
+#include "common.cuh"
+#include "internal.h"
+
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+namespace w4 {
+
+namespace {
+
+__global__ void __launch_bounds__(256)
+hadamard_split_kernel(uint16_t *__restrict__ x2, const uint16_t *__restrict__ x, int K, int b,
+                      int lgb, float norm)
+{
+    extern __shared__ float v[]; // b values of one block
+    pdl_launch_dependents();
+    pdl_wait(); // x may be the previous kernel's output
+    const int m = blockIdx.y;
+    const int k0 = blockIdx.x * b;
+    const uint16_t *xr = x + (size_t)m * K + k0;
+    for (int i = threadIdx.x; i < b; i += blockDim.x)
+        v[i] = bf16lo_to_f32(xr[i]);
+    __syncthreads();
+    // Stage h: pairs (j, j + h) with bit h of j clear; (p, q) -> (p + q, p - q).
+    for (int s = 0; s < lgb; ++s) {
+        const int h = 1 << s;
+        for (int i = threadIdx.x; i < (b >> 1); i += blockDim.x) {
+            const int j = ((i >> s) << (s + 1)) | (i & (h - 1));
+            const float p = v[j], q = v[j + h];
+            v[j] = p + q;
+            v[j + h] = p - q;
+        }
+        __syncthreads();
+    }
+    uint16_t *hi = x2 + (size_t)(2 * m) * K + k0;
+    uint16_t *lo = hi + K;
+    for (int i = threadIdx.x; i < b; i += blockDim.x) {
+        const float r = v[i] * norm;
+        const __nv_bfloat16 h16 = __float2bfloat16_rn(r);
+        hi[i] = __bfloat16_as_ushort(h16);
+        lo[i] = __bfloat16_as_ushort(__float2bfloat16_rn(r - __bfloat162float(h16)));
+    }
+}
+
+} // namespace
+
+cudaError_t run_hadamard_split(uint16_t *x2, const uint16_t *x, int M, int K, int b, cudaStream_t s)
+{
+    int lgb = 0;
+    while ((1 << lgb) < b)
+        ++lgb;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(K / b, M);
+    cfg.blockDim = dim3(b / 2 < 256 ? (b / 2 < 32 ? 32 : b / 2) : 256);
+    cfg.dynamicSmemBytes = (size_t)b * sizeof(float);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float norm = (float)(1.0 / std::sqrt((double)b));
+    return cudaLaunchKernelEx(&cfg, hadamard_split_kernel, x2, x, K, b, lgb, norm);
+}
+
+} // namespace w4

@@ -33,9 +33,11 @@ size_t decode_smem_bytes(const DecodePlan &p, int M, int K);
 // Launches the decode kernel (and, when argmax != nullptr, the argmax pass that
 // reduces keys[M][plan.grid]).
 // lg: log2(group / 32); scales hold one step per 32 << lg codes ([N][K >> (5 + lg)]).
+// pairs: the M x-rows are M/2 (hi, lo) pairs and y has M/2 rows, each the sum of
+// its pair's products (M even; M == 2 or M <= 8 by the plan's kernel).
 cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                        const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
-                       int32_t *argmax, cudaStream_t s);
+                       int32_t *argmax, cudaStream_t s, bool pairs = false);
 
 // Bulk-copy streaming decode kernel (M <= 2, K % 256 == 0, 16-byte aligned
 // codes and steps): cluster size C splits K, nclusters split the row blocks.
@@ -80,6 +82,10 @@ struct PrefillPlan {
 PrefillPlan plan_prefill(int M, int N, int K, int num_sms, size_t ws_floats);
 cudaError_t run_prefill(const PrefillPlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                         const uint16_t *sc, int M, int N, int K, int lg, float *ws, int *err, cudaStream_t s);
+
+// x2[2m] = bf16(v), x2[2m+1] = bf16(v - bf16(v)) for v = (x H)[m], H the block
+// Sylvester-Hadamard matrix with blocks of b (a power of two dividing K), fp32.
+cudaError_t run_hadamard_split(uint16_t *x2, const uint16_t *x, int M, int K, int b, cudaStream_t s);
 
 // Decode attention of one query token (H <= 8 query heads sharing one key/value
 // head, D in {128, 256, 384, 512}) over T cache slots; split partials in ws.

@@ -152,6 +152,26 @@ int w4_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qtable,
 int hbm_read_probe(unsigned long long *sum, const void *buf, size_t bytes, void *stream);
 
 /*
+ * Decode GEMV with Hadamard-rotated weights (source: "fastgemma-gemma-4-E2B"
+ * model card, "What is in the file": every linear weight is rotated along K,
+ * W' = W H^T with H orthogonal, and a runtime fast Walsh-Hadamard transform of
+ * the activation makes the product identical).
+ *
+ *   y[m][n] = sum_k (x H)[m][k] * (code(n,k) - 8) * scale(n, k/group)  (= x W^T)
+ *
+ * qweight/scales hold the rotated weight W' in the usual format; H is
+ * block-diagonal over blocks of `hblock` consecutive k, each the Sylvester
+ * matrix H_b[i][j] = (-1)^popcount(i & j) / sqrt(b). hblock: a power of two in
+ * 2..4096 dividing K. M in 1..4. argmax: NULL, or int32 [M] receiving the lowest
+ * index of each row's maximum (as w4a16_gemv_argmax). x H is formed in fp32 and
+ * carried as two bf16 parts (relative 2^-18), so the decode tolerance holds.
+ * Uses the library's split scratch for the rotated activation (like
+ * w4a16_gemm): calls that need it must not run concurrently on different streams.
+ */
+int w4a16_gemv_hadamard(float *y, int32_t *argmax, const uint16_t *x, const uint32_t *qweight,
+                        const uint16_t *scales, int M, int N, int K, int group, int hblock, void *stream);
+
+/*
  * Decode attention of one query token over a one-head key/value cache (source:
  * "Gemma 4 E2B on a 4 GB GPU with pure PyTorch", decode-attention paragraph: one
  * key/value head serves eight query heads and each cached key and value is read

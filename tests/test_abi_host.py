@@ -83,6 +83,12 @@ def test_validation_before_any_launch(lib):
     # prefill shape rules
     assert l.w4a16_gemm(A, A, A, A, 64, 24, 64, 32, None) == 2
     assert l.w4a16_gemm(A, A, A, A, 64, 32, 96, 32, None) == 2
+    # Hadamard-rotated GEMV: block size, K multiple, rows
+    assert l.w4a16_gemv_hadamard(A, None, A, A, A, 1, 16, 1024, 32, 96, None) == 2
+    assert l.w4a16_gemv_hadamard(A, None, A, A, A, 1, 16, 1024, 32, 8192, None) == 2
+    assert l.w4a16_gemv_hadamard(A, None, A, A, A, 1, 16, 1024, 32, 2048, None) == 1
+    assert l.w4a16_gemv_hadamard(A, None, A, A, A, 5, 16, 1024, 32, 256, None) == 2
+    assert l.w4a16_gemv_hadamard(A, _addr((1 << 20) + 2), A, A, A, 1, 16, 1024, 32, 256, None) == 3
     # decode attention: NULL, sizes, head count / width, alignment
     f = ctypes.c_float(1.0)
     assert l.w4_attn_decode(None, A, A, A, None, 0, 0, 8, 16, 512, f, None) == 1
