@@ -280,7 +280,7 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def measure_rows(w4, dev, stream):
+def measure_rows(w4, dev, stream, sweep=None):
     """Per-row measurements beside the sweep (device time, CUDA events on the
     launching stream; decode calls replayed from a CUDA graph with programmatic
     dependent launch like the sweep; inputs larger than L2 or rotated through
@@ -333,7 +333,44 @@ def measure_rows(w4, dev, stream):
     us = graph_time(lambda: w4.w4a16_gemv_argmax(x, q, sc, out=y, argmax=am, stream=stream), reps=10)
     b = stage_bytes(N, K) + 4
     res["vocab_argmax_262144x1536"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
-    del q, sc
+
+    if sweep is not None:
+        # One token's weight reads: the 140-call sweep then the vocabulary
+        # projection with the greedy pick, in one graph (1184 MiB).
+        def token():
+            sweep.run(w4, stream)
+            w4.w4a16_gemv_argmax(x, q, sc, out=y, argmax=am, stream=stream)
+        us = graph_time(token, reps=10)
+        b = sweep_bytes() + stage_bytes(N, K) + 4
+        res["sweep_plus_vocab"] = {"us": us, "ms": us / 1e3, "GBps": b / us / 1e3, "bytes": b}
+
+        # The same sweep unfused: q, k, v and gate, up as separate calls on row
+        # slices of the fused matrices (245 calls per sweep instead of 140).
+        calls = []
+        for st in sweep.stages:
+            members = next(m for nm, m, _, _ in fused_stages(st["layer"]) if nm == st["name"])
+            r = 0
+            for p in members:
+                n_p = next(n for nm, n, _ in layer_shapes(st["layer"]) if nm == p)
+                calls.append((st["x"], st["qw"][r:r + n_p], st["sc"][r:r + n_p], st["y"][:, r:r + n_p]))
+                r += n_p
+
+        def unfused():
+            for (xx, qq, ss, yy) in calls:
+                w4.w4a16_gemv(xx, qq, ss, out=yy, stream=stream)
+        us = graph_time(unfused, reps=10)
+        b = sum(stage_bytes(qq.shape[0], xx.shape[1]) for (xx, qq, ss, yy) in calls)
+        res["sweep_unfused_245"] = {"us": us, "ms": us / 1e3, "GBps": b / us / 1e3, "bytes": b,
+                                    "calls": len(calls)}
+
+    # The LM head as the fastgemma card stores it: Hadamard-rotated, group 256,
+    # with the activation's transform (blocks of 512) and the greedy pick.
+    sc256 = dev16(synth.gen_scales(1000, N, K, 256))
+    us = graph_time(lambda: w4.w4a16_gemv_hadamard(x, q, sc256, 512, group=256, out=y, argmax=am,
+                                                   stream=stream), reps=10)
+    b = N * K // 2 + N * (K // 256) * 2 + 2 * K + 4 * N + 4
+    res["vocab_hadamard_g256_b512_argmax"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    del q, sc, sc256
 
     # M=8 decode sweep: the sweep's shapes with 8 x-rows per call.
     sw8 = Sweep(dev, keep_host=False, m=8)
@@ -508,7 +545,7 @@ def run_ours(args, rank, world):
     del probe_buf
     torch.cuda.empty_cache()
 
-    rows = measure_rows(w4, dev, stream) if args.rows else None
+    rows = measure_rows(w4, dev, stream, sweep) if args.rows else None
 
     # End to end through the public call with host buffers: every step copies
     # the sweep's packed weights, steps and x from pinned host memory and reads
