@@ -473,6 +473,23 @@ def captured_traffic():
         return None
 
 
+def max_over_ranks(t_ms: float, world: int, device) -> float:
+    """The slowest rank's time (all_reduce MAX over the default process group when
+    world > 1): the job's time, as every rank sees it."""
+    if world <= 1:
+        return t_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([t_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(t_ms: float, nbytes: int, world: int) -> float:
+    """Whole-job GB/s: every rank moved nbytes in the slowest rank's time."""
+    return world * nbytes / (t_ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -522,12 +539,8 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    t_ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([t_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_ms = float(t.item())
-    value = world * nbytes / (t_ms * 1e-3) / 1e9
+    t_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    value = job_rate(t_ms, nbytes, world)
 
     # In-run read ceiling: the plain-sum probe over a 4 GiB buffer.
     probe_buf = torch.empty(1 << 30, dtype=torch.int32, device=dev)
@@ -598,12 +611,8 @@ def run_ours(args, rank, world):
             stream.wait_stream(cs)
         q1.record(stream)
         torch.cuda.synchronize()
-        te = q0.elapsed_time(q1) / e2e_steps
-        if world > 1:
-            t = torch.tensor([te], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            te = float(t.item())
-        e2e = {"value": world * nbytes / (te * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": te,
+        te = max_over_ranks(q0.elapsed_time(q1) / e2e_steps, world, dev)
+        e2e = {"value": job_rate(te, nbytes, world), "unit": "GB/s", "ms_per_step": te,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     cpu = None
