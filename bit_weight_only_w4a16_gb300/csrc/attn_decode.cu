@@ -104,18 +104,26 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
     return l | (h << 16);
 }
 
-template <int NW, int kRing>
-__global__ void __launch_bounds__(NW * 32)
+// GR groups of NW warps per CTA: group gi streams the gi-th half of the CTA's
+// tiles with its own online-softmax state; the groups' states are merged in
+// shared memory so the CTA stores one slice partial.
+template <int NW, int kRing, int GR>
+__global__ void __launch_bounds__(GR * NW * 32)
 attn_split_kernel(const AttnArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int gi = w / NW, wl = w - gi * NW; // group, warp within the group
     const int g = lane >> 2, tq = lane & 3;
     const uint32_t ring = smem_addr(smem) + w * kRing * kSlot;
-    float *sp = reinterpret_cast<float *>(smem + NW * kRing * kSlot); // [2][NW][16 tokens][8 heads]
-    const int tile0 = (int)((long long)blockIdx.x * a.ntiles / gridDim.x);
-    const int nt = (int)((long long)(blockIdx.x + 1) * a.ntiles / gridDim.x) - tile0;
-    const int d0 = w * kDW;
+    // [GR][2][NW][16 tokens][8 heads]
+    float *sp = reinterpret_cast<float *>(smem + GR * NW * kRing * kSlot) + gi * 2 * NW * 128;
+    const int ctile0 = (int)((long long)blockIdx.x * a.ntiles / gridDim.x);
+    const int cnt = (int)((long long)(blockIdx.x + 1) * a.ntiles / gridDim.x) - ctile0;
+    const int nt0 = (cnt + 1) >> 1;
+    const int tile0 = GR == 1 ? ctile0 : ctile0 + (gi ? nt0 : 0);
+    const int nt = GR == 1 ? cnt : (gi ? cnt - nt0 : nt0);
+    const int d0 = wl * kDW;
 
     pdl_launch_dependents();
     pdl_wait(); // the query and the cache may be written by the previous kernel
@@ -179,14 +187,14 @@ attn_split_kernel(const AttnArgs a)
         }
         float *spb = sp + (i & 1) * NW * 128;
         {
-            float *mine = spb + w * 128;
+            float *mine = spb + wl * 128;
             mine[g * 8 + 2 * tq] = c0[0] + c1[0];
             mine[g * 8 + 2 * tq + 1] = c0[1] + c1[1];
             mine[(g + 8) * 8 + 2 * tq] = c0[2] + c1[2];
             mine[(g + 8) * 8 + 2 * tq + 1] = c0[3] + c1[3];
         }
         if (NW > 1)
-            named_sync(1, NW * 32);
+            named_sync(1 + gi, NW * 32);
         else
             __syncwarp();
 
@@ -242,6 +250,40 @@ attn_split_kernel(const AttnArgs a)
     }
     cp_async_wait_group<0>(); // only empty groups remain
 
+    if (GR == 2) {
+        // Group 1 leaves its state in its own (finished) ring; group 0 merges:
+        // m = max(m0, m1), each side scaled by 2^(m_i - m).
+        float *park = reinterpret_cast<float *>(smem + (size_t)(NW + wl) * kRing * kSlot) + lane * 34;
+        if (gi == 1) {
+#pragma unroll
+            for (int s2 = 0; s2 < 8; ++s2)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    park[s2 * 4 + c] = o[s2][c];
+            park[32] = m_run;
+            park[33] = l_run;
+        }
+        __syncthreads();
+        if (gi == 1)
+            return;
+        const float m1 = park[32], l1 = park[33];
+        const float mm = fmaxf(m_run, m1);
+        const float f0 = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mm);
+        const float f1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - mm);
+        l_run = l_run * f0 + l1 * f1;
+        m_run = mm;
+        // o holds heads 2tq, 2tq+1, whose factors live on lanes 8tq and 8tq+4.
+        const float a0 = __shfl_sync(0xFFFFFFFFu, f0, 8 * tq), a1 = __shfl_sync(0xFFFFFFFFu, f0, 8 * tq + 4);
+        const float b0 = __shfl_sync(0xFFFFFFFFu, f1, 8 * tq), b1 = __shfl_sync(0xFFFFFFFFu, f1, 8 * tq + 4);
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+            o[s2][0] = o[s2][0] * a0 + park[s2 * 4 + 0] * b0;
+            o[s2][1] = o[s2][1] * a1 + park[s2 * 4 + 1] * b1;
+            o[s2][2] = o[s2][2] * a0 + park[s2 * 4 + 2] * b0;
+            o[s2][3] = o[s2][3] * a1 + park[s2 * 4 + 3] * b1;
+        }
+    }
+
     // Unnormalised slice outputs, running max and sum (heads >= H are unused).
     float *wo = a.ws_o + (size_t)blockIdx.x * kHeads * a.D;
 #pragma unroll
@@ -252,7 +294,7 @@ attn_split_kernel(const AttnArgs a)
         wo[(size_t)(2 * tq) * a.D + d + 8] = o[s][2];
         wo[(size_t)(2 * tq + 1) * a.D + d + 8] = o[s][3];
     }
-    if (w == 0 && tq == 0) {
+    if (wl == 0 && tq == 0) {
         a.ws_ml[((size_t)blockIdx.x * kHeads + g) * 2] = m_run;
         a.ws_ml[((size_t)blockIdx.x * kHeads + g) * 2 + 1] = l_run;
     }
@@ -330,13 +372,14 @@ cudaError_t launch_attn(const AttnArgs &a0, float *out, float *ws, size_t ws_flo
     // slots x 512: depth 2 / 3 / 4 / 6 (3 / 2 / 1 / 1 CTAs per SM) took
     // 53.4 / 50.5 / 67.7 / 69.9 us; warps per SM matter more than depth.
     constexpr int R = 3;
-    auto kern = attn_split_kernel<NW, R>;
-    const size_t smem = (size_t)NW * R * kSlot + 2 * (size_t)NW * 128 * sizeof(float);
+    constexpr int GR = NW == 4 ? 2 : 1; // one CTA of 8 warps per SM at D = 512
+    auto kern = attn_split_kernel<NW, R, GR>;
+    const size_t smem = (size_t)GR * NW * R * kSlot + (size_t)GR * 2 * NW * 128 * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NW * 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, GR * NW * 32, smem);
     if (e != cudaSuccess)
         return e;
     if (occ < 1)
@@ -359,7 +402,7 @@ cudaError_t launch_attn(const AttnArgs &a0, float *out, float *ws, size_t ws_flo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nsplit);
-    cfg.blockDim = dim3(NW * 32);
+    cfg.blockDim = dim3(GR * NW * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
