@@ -660,6 +660,8 @@ def run_ncu_case(case: str):
     gather_probe  : w4_embed_gather of 8 ids from the 262144 x 8960 table and
                     hbm_read_probe over 1 GiB, twice each.
     attn          : w4_attn_decode twice over a 131072-slot x 512 cache (8 heads).
+    hadamard      : w4a16_gemv_hadamard (blocks of 512, group 256, argmax) twice on
+                    the 262144 x 1536 vocabulary projection.
     prefill:NxK   : w4a16_gemm twice with M=1024 tokens on an N x K weight.
     """
     import torch
@@ -676,7 +678,14 @@ def run_ncu_case(case: str):
         sc = torch.from_numpy(synth.gen_scales(seed, N, K).view(np.int16)).to(dev)
         return x, q, sc
 
-    if case == "attn":
+    if case == "hadamard":
+        N, K = 262144, 1536
+        q = synth.gen_qweight_torch(1000, N, K, dev)
+        sc = torch.from_numpy(synth.gen_scales(1000, N, K, 256).view(np.int16)).to(dev)
+        x = torch.from_numpy(synth.gen_x(1000, 1, K).view(np.int16)).to(dev)
+        for _ in range(2):
+            w4.w4a16_gemv_hadamard(x, q, sc, 512, group=256, argmax=True)
+    elif case == "attn":
         H, T, D = 8, 131072, 512
         q = torch.from_numpy(synth.gen_attn_q(404, H, D).view(np.int16)).to(dev)
         kh, vh = synth.gen_attn_kv(404, T, D)
@@ -735,7 +744,7 @@ def main():
                          "gather, prefill)")
     ap.add_argument("--ncu-case", default=None,
                     help="run one small fixed case for an ncu capture instead of the bench: "
-                         "decode_shapes | m8_shapes | vocab | gather_probe | attn | prefill:NxK")
+                         "decode_shapes | m8_shapes | vocab | gather_probe | attn | hadamard | prefill:NxK")
     args = ap.parse_args()
     if args.ncu_case:
         run_ncu_case(args.ncu_case)
