@@ -193,3 +193,74 @@ def gemm_xf64(x, qweight, scales, group: int = 32, rows=None):
 def gemm_hadamard(x, qweight, scales, hblock: int, group: int = 32, rows=None):
     """(y, absy): the rotated product (x H) W'^T with W' = dequant(qweight, scales)."""
     return gemm_xf64(hadamard(x, hblock), qweight, scales, group, rows)
+
+
+# ----------------------------------------------------------------------------
+# Device-resident decode-step plumbing (reading R18). Sources: "Gemma 4 E2B on a
+# 4 GB GPU with pure PyTorch" - the cache paragraph (full layers: one slot per
+# position; sliding layers: a ring of slots recording each slot's position), the
+# CUDA-graph paragraph (every position kept on the GPU so that one captured step
+# replays for every token), the emb4 paragraph (embedding and LM head share one
+# 4-bit table) and the tool-calling paragraph (a step whose constrained decoder
+# admits one token skips the LM-head read).
+#
+# R18: the token at position p appends its key/value rows to slot p mod T of a
+# ring (which records p) or slot p of a full cache before its attention runs;
+# the step's LM head yields the token at position p + 1, either the greedy pick
+# or the forced token (then no logits are formed); the prologue records it in
+# the history at index p + 1, advances the position to p + 1 and looks up its
+# embedding row (the plain 4-bit gather, no model-specific scaling).
+# ----------------------------------------------------------------------------
+
+def kv_append(k_cache, v_cache, kpos, k_new, v_new, pos: int):
+    """(k_cache', v_cache', kpos', status) after appending position `pos`.
+
+    kpos int32 [T] (ring) or None (full cache). Ring: slot pos mod T, whose
+    recorded position becomes pos. Full cache: slot pos, which must lie in
+    [0, T). A negative position, or one outside a full cache, changes nothing
+    and gives status 1.
+    """
+    k_cache = np.array(k_cache, dtype=np.uint16, copy=True)
+    v_cache = np.array(v_cache, dtype=np.uint16, copy=True)
+    kp = None if kpos is None else np.array(kpos, dtype=np.int32, copy=True)
+    T = k_cache.shape[0]
+    pos = int(pos)
+    if pos < 0 or (kp is None and pos >= T):
+        return k_cache, v_cache, kp, 1
+    slot = pos % T if kp is not None else pos
+    k_cache[slot] = np.asarray(k_new, dtype=np.uint16).ravel()
+    v_cache[slot] = np.asarray(v_new, dtype=np.uint16).ravel()
+    if kp is not None:
+        kp[slot] = pos
+    return k_cache, v_cache, kp, 0
+
+
+def lm_head_pick(x, qweight, scales, group: int, forced: int):
+    """(token, y, absy): the forced token when forced >= 0 (y, absy None: no logits
+    are formed), else the greedy pick, the lowest index of the largest logit of
+    the one x-row (y, absy from gemm())."""
+    if int(forced) >= 0:
+        return int(forced), None, None
+    y, a = gemm(x, qweight, scales, group)
+    return argmax(y[0])[0], y, a
+
+
+def decode_prologue(token: int, pos: int, tokens, qtable, scales, group: int = 32):
+    """(x_next bf16 bits [1][K], tokens', pos + 1, status) of the next-step prologue.
+
+    tokens: int32 history (or None); the token is stored at index pos + 1 when
+    that index lies inside it (else status bit 1). A token outside the table
+    gives a zero row and status bit 0 (the gather's own rule).
+    """
+    status = 0
+    tk = None if tokens is None else np.array(tokens, dtype=np.int32, copy=True)
+    nx = int(pos) + 1
+    if tk is not None:
+        if 0 <= nx < tk.shape[0]:
+            tk[nx] = int(token)
+        else:
+            status |= 2
+    row, flag = embed_gather(np.array([int(token)], dtype=np.int32), qtable, scales, group)
+    if flag:
+        status |= 1
+    return row, tk, nx, status
