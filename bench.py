@@ -370,7 +370,41 @@ def measure_rows(w4, dev, stream, sweep=None):
                                                    stream=stream), reps=10)
     b = N * K // 2 + N * (K // 256) * 2 + 2 * K + 4 * N + 4
     res["vocab_hadamard_g256_b512_argmax"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
-    del q, sc, sc256
+
+    # Device-resident step plumbing on the tied 262144 x 1536 group-256 table
+    # (embedding and LM head share it): the greedy LM head with and without a
+    # forced token (a forced step reads no weight), the next-step prologue
+    # (history, position, the token's embedding row) and, with the sweep, whole
+    # token steps in both modes.
+    forced = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    pos = torch.zeros((1,), dtype=torch.int32, device=dev)
+    hist = torch.zeros((1 << 20,), dtype=torch.int32, device=dev)
+    xn = torch.empty((1, K), dtype=torch.bfloat16, device=dev)
+
+    def head():
+        w4.w4a16_gemv_argmax_forced(x, q, sc256, forced, group=256, out=y, argmax=am, stream=stream)
+
+    def prologue():
+        w4.w4_decode_prologue(am, pos, q, sc256, group=256, x_next=xn, tokens=hist, stream=stream)
+
+    b = N * K // 2 + N * (K // 256) * 2 + 2 * K + 4 * N + 4
+    us = graph_time(head, reps=10)
+    res["lm_head_g256_greedy"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    forced.fill_(7)
+    us = graph_time(lambda: [head() for _ in range(20)], reps=10) / 20
+    res["lm_head_g256_forced_skip"] = {"us": us, "bytes_read": 4}
+    us = graph_time(lambda: [prologue() for _ in range(50)], reps=10) / 50
+    pos.zero_()
+    res["decode_prologue_1536_g256"] = {"us": us, "bytes": K // 2 + (K // 256) * 2 + 2 * K + 16}
+    if sweep is not None:
+        forced.fill_(-1)
+        us = graph_time(lambda: (sweep.run(w4, stream), head(), prologue()), reps=10)
+        res["token_step_greedy"] = {"us": us, "ms": us / 1e3}
+        forced.fill_(7)
+        us = graph_time(lambda: (sweep.run(w4, stream), head(), prologue()), reps=10)
+        res["token_step_forced"] = {"us": us, "ms": us / 1e3}
+        pos.zero_()
+    del q, sc, sc256, hist
 
     # M=8 decode sweep: the sweep's shapes with 8 x-rows per call.
     sw8 = Sweep(dev, keep_host=False, m=8)
@@ -417,6 +451,13 @@ def measure_rows(w4, dev, stream, sweep=None):
                                                out=out, stream=stream) for c in range(copies)], reps=5) / copies
     b = 2 * T * D * 2 + H * D * 2 + H * D * 4 + T * 4
     res["attn_ring_512x256"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    # The sliding layer's append at a device position (ring slot of *pos).
+    kn = k1[0].clone()
+    vn = v1[0].clone()
+    posd = torch.full((1,), 70001, dtype=torch.int32, device=dev)
+    us = graph_time(lambda: [w4.w4_kv_append(ks[c], vs[c], kn, vn, posd, kpos=kp, stream=stream)
+                             for c in range(64)], reps=10) / 64
+    res["kv_append_ring_512x256"] = {"us": us, "bytes": 4 * D * 2 + 8}
     del ks, vs, k1, v1
 
     # Prefill GEMM, 1024 tokens, tensor-core bound: 8 weight copies rotated.

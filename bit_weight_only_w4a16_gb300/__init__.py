@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "W4_OK", 1: "W4_ERR_INVALID_ARG", 2: "W4_ERR_UNSUPPORTED",
 # Symbols declared in include/w4a16.h.
 EXPORTS = ("w4_status_string", "w4_last_cuda_error", "w4_init", "w4_device_error", "w4a16_gemv", "w4a16_gemm",
            "w4a16_gemv_argmax", "w4a16_gemv_argmax_noalloc", "w4_embed_gather", "hbm_read_probe",
-           "w4_attn_decode", "w4a16_gemv_hadamard")
+           "w4_attn_decode", "w4a16_gemv_hadamard", "w4_selftest_wait_timeout", "w4_attn_decode_devpos",
+           "w4_kv_append", "w4a16_gemv_argmax_forced", "w4_decode_prologue")
 
 
 class W4Error(RuntimeError):
@@ -65,6 +66,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.w4_attn_decode.restype = I
     lib.w4a16_gemv_hadamard.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
     lib.w4a16_gemv_hadamard.restype = I
+    lib.w4_selftest_wait_timeout.argtypes = [P]
+    lib.w4_selftest_wait_timeout.restype = I
+    lib.w4_attn_decode_devpos.argtypes = [P, P, P, P, P, P, I, I, I, I, ctypes.c_float, P]
+    lib.w4_attn_decode_devpos.restype = I
+    lib.w4_kv_append.argtypes = [P, P, P, P, P, P, I, I, P, P]
+    lib.w4_kv_append.restype = I
+    lib.w4a16_gemv_argmax_forced.argtypes = [P, P, P, P, P, I, I, I, P, P]
+    lib.w4a16_gemv_argmax_forced.restype = I
+    lib.w4_decode_prologue.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P]
+    lib.w4_decode_prologue.restype = I
     return lib
 
 
@@ -202,7 +213,8 @@ def w4_attn_decode(q, k, v, kpos=None, qpos=None, window: int = 0, scale: float 
 
     q bf16 [H][D] (H <= 8 query heads sharing the key/value head); k, v bf16 [T][D];
     kpos int32 [T] (position recorded in each slot, -1 = empty) or None (slot t
-    holds position t); qpos defaults to T - 1; window 0 = no window.
+    holds position t); qpos defaults to T - 1, or is a device int32 [1] tensor read
+    when the kernels run (w4_attn_decode_devpos); window 0 = no window.
     """
     _bits16(q, "q"); _bits16(k, "k"); _bits16(v, "v")
     H, D = q.shape
@@ -213,8 +225,15 @@ def w4_attn_decode(q, k, v, kpos=None, qpos=None, window: int = 0, scale: float 
         _cuda(kpos, "kpos")
         if kpos.dtype != torch.int32 or kpos.numel() != T:
             raise ValueError("kpos must be int32 [T]")
-    qp = T - 1 if qpos is None else int(qpos)
     o = torch.empty((H, D), dtype=torch.float32, device=q.device) if out is None else _cuda(out, "out")
+    if isinstance(qpos, torch.Tensor):
+        _cuda(qpos, "qpos")
+        if qpos.dtype != torch.int32 or qpos.numel() != 1:
+            raise ValueError("a device qpos must be int32 [1]")
+        _check(_lib.w4_attn_decode_devpos(_ptr(o), _ptr(q), _ptr(k), _ptr(v), _ptr(kpos), _ptr(qpos), int(window),
+                                          H, T, D, float(scale), _stream(stream)), "w4_attn_decode_devpos")
+        return o
+    qp = T - 1 if qpos is None else int(qpos)
     _check(_lib.w4_attn_decode(_ptr(o), _ptr(q), _ptr(k), _ptr(v), _ptr(kpos), qp, int(window), H, T, D,
                                float(scale), _stream(stream)), "w4_attn_decode")
     return o
@@ -235,3 +254,63 @@ def w4a16_gemv_hadamard(x, qweight, scales, hblock: int, group: int = 32, out=No
     _check(_lib.w4a16_gemv_hadamard(_ptr(y), _ptr(a), _ptr(x), _ptr(qweight), _ptr(scales), M, N, K, group,
                                     int(hblock), _stream(stream)), "w4a16_gemv_hadamard")
     return (y, a) if a is not None else y
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Launch the failure-path self-test: a kernel whose bounded wait cannot
+    complete gives up and sets bit 2 of the device error word (device_error())."""
+    _check(_lib.w4_selftest_wait_timeout(_stream(stream)), "w4_selftest_wait_timeout")
+
+
+def _i32_scalar(t, name):
+    _cuda(t, name)
+    if t.dtype != torch.int32 or t.numel() < 1:
+        raise ValueError(f"{name} must be a device int32 tensor")
+    return t
+
+
+def w4_kv_append(k_cache, v_cache, k_new, v_new, pos, kpos=None, status=None, stream=None):
+    """Write k_new, v_new (bf16 [D]) into slot *pos mod T of a ring (kpos int32 [T]
+    records *pos there) or slot *pos of a full cache (kpos None)."""
+    _bits16(k_cache, "k_cache"); _bits16(v_cache, "v_cache"); _bits16(k_new, "k_new"); _bits16(v_new, "v_new")
+    _i32_scalar(pos, "pos")
+    T, D = k_cache.shape
+    if tuple(v_cache.shape) != (T, D) or k_new.numel() != D or v_new.numel() != D:
+        raise ValueError("cache / new-row shape mismatch")
+    if kpos is not None and (kpos.dtype != torch.int32 or kpos.numel() != T):
+        raise ValueError("kpos must be int32 [T]")
+    _check(_lib.w4_kv_append(_ptr(k_cache), _ptr(v_cache), _ptr(kpos), _ptr(k_new), _ptr(v_new), _ptr(pos), T, D,
+                             _ptr(status), _stream(stream)), "w4_kv_append")
+
+
+def w4a16_gemv_argmax_forced(x, qweight, scales, forced, group: int = 32, out=None, argmax=None, stream=None):
+    """Greedy LM head for one x-row; when the device int32 *forced >= 0 no weight is
+    read, y is left unchanged and argmax[0] = *forced. Returns (y, argmax)."""
+    _bits16(x, "x"); _u32(qweight, "qweight"); _bits16(scales, "scales")
+    _i32_scalar(forced, "forced")
+    M, N, K = _shape(x, qweight, scales, group)
+    if M != 1:
+        raise ValueError("the forced-token LM head takes one x-row")
+    y = torch.empty((1, N), dtype=torch.float32, device=x.device) if out is None else _cuda(out, "out")
+    a = torch.empty((1,), dtype=torch.int32, device=x.device) if argmax is None else _i32_scalar(argmax, "argmax")
+    _check(_lib.w4a16_gemv_argmax_forced(_ptr(y), _ptr(a), _ptr(x), _ptr(qweight), _ptr(scales), N, K, group,
+                                         _ptr(forced), _stream(stream)), "w4a16_gemv_argmax_forced")
+    return y, a
+
+
+def w4_decode_prologue(token, pos, qtable, scales, group: int = 32, x_next=None, tokens=None, status=None,
+                       stream=None):
+    """tok = *token; tokens[*pos + 1] = tok; *pos += 1; x_next = bf16 row tok of the
+    4-bit table (as w4_embed_gather). Returns x_next (bf16 [1][K])."""
+    _i32_scalar(token, "token"); _i32_scalar(pos, "pos"); _u32(qtable, "qtable"); _bits16(scales, "scales")
+    V, K = qtable.shape[0], qtable.shape[1] * 8
+    if tuple(scales.shape) != (V, K // group):
+        raise ValueError("scales shape mismatch")
+    cap = 0
+    if tokens is not None:
+        _i32_scalar(tokens, "tokens")
+        cap = tokens.numel()
+    o = torch.empty((1, K), dtype=torch.bfloat16, device=token.device) if x_next is None else _cuda(x_next, "x_next")
+    _check(_lib.w4_decode_prologue(_ptr(o), _ptr(tokens), _ptr(pos), _ptr(token), _ptr(qtable), _ptr(scales), V, K,
+                                   group, cap, _ptr(status), _stream(stream)), "w4_decode_prologue")
+    return o

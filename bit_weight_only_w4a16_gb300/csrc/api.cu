@@ -103,6 +103,23 @@ int device_state(DeviceState **out)
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+int check_attn_args(const float *out, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    const int32_t *kpos, int window, int H, int T, int D)
+{
+    if (!out || !q || !k || !v)
+        return W4_ERR_INVALID_ARG;
+    if (H < 1 || T < 1 || D < 1 || window < 0)
+        return W4_ERR_INVALID_ARG;
+    if (H > 8 || D % 128 != 0 || D > 512)
+        return W4_ERR_UNSUPPORTED;
+    if ((long long)T * D >= (1ll << 31))
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 4) ||
+        (kpos && !aligned(kpos, 4)))
+        return W4_ERR_MISALIGNED;
+    return W4_OK;
+}
+
 int check_w4_args(const void *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int M,
                   int N, int K, int group)
 {
@@ -310,23 +327,14 @@ int w4_attn_decode(float *out, const uint16_t *q, const uint16_t *k, const uint1
                    const int32_t *kpos, int qpos, int window, int H, int T, int D, float scale,
                    void *stream)
 {
-    if (!out || !q || !k || !v)
-        return W4_ERR_INVALID_ARG;
-    if (H < 1 || T < 1 || D < 1 || window < 0)
-        return W4_ERR_INVALID_ARG;
-    if (H > 8 || D % 128 != 0 || D > 512)
-        return W4_ERR_UNSUPPORTED;
-    if ((long long)T * D >= (1ll << 31))
-        return W4_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 4) ||
-        (kpos && !aligned(kpos, 4)))
-        return W4_ERR_MISALIGNED;
-    DeviceState *st = nullptr;
-    int rc = device_state(&st);
+    int rc = check_attn_args(out, q, k, v, kpos, window, H, T, D);
     if (rc != W4_OK)
         return rc;
-    cudaError_t e = w4::run_attn_decode(out, q, k, v, kpos, qpos, window, H, T, D, scale, st->ws, kWsFloats,
-                                        st->num_sms, static_cast<cudaStream_t>(stream));
+    DeviceState *st = nullptr;
+    if ((rc = device_state(&st)) != W4_OK)
+        return rc;
+    cudaError_t e = w4::run_attn_decode(out, q, k, v, kpos, qpos, nullptr, window, H, T, D, scale, st->ws,
+                                        kWsFloats, st->num_sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 
@@ -359,6 +367,101 @@ int w4a16_gemv_hadamard(float *y, int32_t *argmax, const uint16_t *x, const uint
     if (e == cudaSuccess)
         e = w4::run_decode(p, y, x2, qweight, scales, 2 * M, N, K, w4::group_shift(group),
                            argmax ? st->keys : nullptr, argmax, s, true);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int w4_selftest_wait_timeout(void *stream)
+{
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != W4_OK)
+        return rc;
+    cudaError_t e = w4::run_bounded_wait_selftest(st->err, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int w4_attn_decode_devpos(float *out, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const int32_t *kpos, const int32_t *qpos, int window, int H, int T, int D,
+                          float scale, void *stream)
+{
+    int rc = check_attn_args(out, q, k, v, kpos, window, H, T, D);
+    if (rc != W4_OK)
+        return rc;
+    if (!qpos)
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(qpos, 4))
+        return W4_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    if ((rc = device_state(&st)) != W4_OK)
+        return rc;
+    cudaError_t e = w4::run_attn_decode(out, q, k, v, kpos, 0, qpos, window, H, T, D, scale, st->ws, kWsFloats,
+                                        st->num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int w4_kv_append(uint16_t *k_cache, uint16_t *v_cache, int32_t *kpos, const uint16_t *k_new,
+                 const uint16_t *v_new, const int32_t *pos, int T, int D, int32_t *status, void *stream)
+{
+    if (!k_cache || !v_cache || !k_new || !v_new || !pos)
+        return W4_ERR_INVALID_ARG;
+    if (T < 1 || D < 8 || D % 8 != 0 || (long long)T * D >= (1ll << 31))
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+        !aligned(pos, 4) || (kpos && !aligned(kpos, 4)) || (status && !aligned(status, 4)))
+        return W4_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != W4_OK)
+        return rc;
+    cudaError_t e = w4::run_kv_append(k_cache, v_cache, kpos, k_new, v_new, const_cast<int32_t *>(pos), T, D,
+                                      status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int w4a16_gemv_argmax_forced(float *y, int32_t *argmax, const uint16_t *x, const uint32_t *qweight,
+                             const uint16_t *scales, int N, int K, int group, const int32_t *forced,
+                             void *stream)
+{
+    int rc = check_w4_args(y, x, qweight, scales, 1, N, K, group);
+    if (rc != W4_OK)
+        return rc;
+    if (!argmax || !forced)
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(argmax, 4) || !aligned(forced, 4))
+        return W4_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    if ((rc = device_state(&st)) != W4_OK)
+        return rc;
+    const w4::DecodePlan p = w4::plan_decode(1, N, K, st->num_sms);
+    if (p.kernel == 8 || !decode_fits(p, 1, K) || (size_t)p.grid > kKeyCapacity)
+        return W4_ERR_UNSUPPORTED;
+    cudaError_t e = w4::run_decode(p, y, x, qweight, scales, 1, N, K, w4::group_shift(group), st->keys, argmax,
+                                   static_cast<cudaStream_t>(stream), false, forced);
+    return e == cudaSuccess ? W4_OK : cuda_fail(e);
+}
+
+int w4_decode_prologue(uint16_t *x_next, int32_t *tokens, int32_t *pos, const int32_t *token,
+                       const uint32_t *qtable, const uint16_t *scales, int V, int K, int group, int cap,
+                       int32_t *status, void *stream)
+{
+    if (!x_next || !pos || !token || !qtable || !scales)
+        return W4_ERR_INVALID_ARG;
+    if (V < 1 || K < 1 || (tokens && cap < 1))
+        return W4_ERR_INVALID_ARG;
+    if (w4::group_shift(group) < 0)
+        return W4_ERR_UNSUPPORTED;
+    if (K % group != 0 || (long long)V * (K / 8) >= (1ll << 31))
+        return W4_ERR_INVALID_ARG;
+    if (!aligned(x_next, 16) || !aligned(qtable, 4) || !aligned(scales, 2) || !aligned(pos, 4) ||
+        !aligned(token, 4) || (tokens && !aligned(tokens, 4)) || (status && !aligned(status, 4)))
+        return W4_ERR_MISALIGNED;
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != W4_OK)
+        return rc;
+    cudaError_t e = w4::run_decode_prologue(x_next, tokens, pos, token, qtable, scales, V, K,
+                                            w4::group_shift(group), tokens ? cap : 0, status,
+                                            static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 

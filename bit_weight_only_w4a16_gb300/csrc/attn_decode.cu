@@ -28,7 +28,13 @@
 //   - values: mma with the warp's 16 head dims as rows and the 8 heads as
 //     columns (A = value tile transposed by ldmatrix.trans, B = the weights);
 //   - each CTA stores its unnormalised output with its running max and sum; a
-//     second kernel merges the slices in a fixed order (deterministic).
+//     second kernel merges the slices in a fixed order (deterministic);
+//   - the query position may live in device memory ("with every position on
+//     the GPU", the cache paragraph): it is read after the wait on the previous
+//     kernel, so one captured graph serves every decode step. Without a slot
+//     table (slot t holds position t) a CTA drops the tiles that hold no kept
+//     position; such tiles add nothing (zero weights, unchanged running max),
+//     so the result is bitwise the same as streaming them.
 // Shared-memory tiles are [16 tokens][128 dims] with 16-byte chunk c of row r
 // stored at chunk c ^ (r & 7), so both ldmatrix forms read conflict-free.
 #include "common.cuh"
@@ -52,16 +58,18 @@ struct AttnArgs {
     float *ws_o;  // [nsplit][8][D] unnormalised outputs
     float *ws_ml; // [nsplit][8][2] running max (log2 domain) and sum
     long long qpos, lo; // kept positions: lo < p <= qpos (lo = -1 without a window)
+    const int32_t *qpos_dev; // when set: qpos = *qpos_dev at run time, lo from `window`
+    long long window;
     int H, T, D, ntiles;
     float scale_log2; // scale * log2(e)
 };
 
-__device__ __forceinline__ bool slot_kept(const AttnArgs &a, int tok)
+__device__ __forceinline__ bool slot_kept(const AttnArgs &a, int tok, long long qpos, long long lo)
 {
     if (tok >= a.T)
         return false;
     const long long p = a.kpos ? (long long)__ldg(a.kpos + tok) : (long long)tok;
-    return p >= 0 && p <= a.qpos && p > a.lo;
+    return p >= 0 && p <= qpos && p > lo;
 }
 
 // 16-byte cp.async that writes zeros instead of reading when !valid.
@@ -121,12 +129,28 @@ attn_split_kernel(const AttnArgs a)
     const int ctile0 = (int)((long long)blockIdx.x * a.ntiles / gridDim.x);
     const int cnt = (int)((long long)(blockIdx.x + 1) * a.ntiles / gridDim.x) - ctile0;
     const int nt0 = (cnt + 1) >> 1;
-    const int tile0 = GR == 1 ? ctile0 : ctile0 + (gi ? nt0 : 0);
-    const int nt = GR == 1 ? cnt : (gi ? cnt - nt0 : nt0);
+    int tile0 = GR == 1 ? ctile0 : ctile0 + (gi ? nt0 : 0);
+    int nt = GR == 1 ? cnt : (gi ? cnt - nt0 : nt0);
     const int d0 = wl * kDW;
 
     pdl_launch_dependents();
-    pdl_wait(); // the query and the cache may be written by the previous kernel
+    pdl_wait(); // the query, the cache and the position may be written by the previous kernel
+
+    long long qpos = a.qpos, lo = a.lo;
+    if (a.qpos_dev != nullptr) {
+        qpos = (long long)*a.qpos_dev;
+        lo = a.window > 0 ? qpos - a.window : -1;
+    }
+    if (a.kpos == nullptr) {
+        // Kept slots lie in [lo + 1, min(qpos, T - 1)]: only tiles [ft, et) hold any.
+        const long long last = qpos < (long long)a.T - 1 ? qpos : (long long)a.T - 1;
+        const long long ft = lo < 0 ? 0 : (lo + 1) / kTok;
+        const long long et = last < 0 ? 0 : last / kTok + 1;
+        const long long b = tile0 > ft ? tile0 : ft;
+        const long long e = (long long)tile0 + nt < et ? (long long)tile0 + nt : et;
+        tile0 = (int)(b < e ? b : tile0);
+        nt = (int)(b < e ? e - b : 0);
+    }
 
     // Query as the score mma's B operand: head g, dims d0 + 16 s + 2 tq (+1) and + 8 (+9).
     uint32_t qb[8][2];
@@ -147,7 +171,7 @@ attn_split_kernel(const AttnArgs a)
 #pragma unroll
             for (int c = lane; c < kTok * 16; c += 32) {
                 const int r = c >> 4, j = c & 15;
-                const bool ok = slot_kept(a, tb + r);
+                const bool ok = slot_kept(a, tb + r, qpos, lo);
                 const size_t off = (size_t)(ok ? tb + r : 0) * a.D + d0 + j * 8;
                 const uint32_t so = r * 256 + ((j ^ (r & 7)) << 4);
                 cp_async16_zfill(kb + so, a.k + off, ok);
@@ -209,7 +233,7 @@ attn_split_kernel(const AttnArgs a)
 #pragma unroll
             for (int u = 0; u < NW; ++u)
                 acc += spb[u * 128 + tok * 8 + g];
-            sc[j] = slot_kept(a, tb + tok) ? acc * a.scale_log2 : -INFINITY;
+            sc[j] = slot_kept(a, tb + tok, qpos, lo) ? acc * a.scale_log2 : -INFINITY;
         }
         float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
         tmax = fmaxf(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, 1));
@@ -425,8 +449,9 @@ cudaError_t launch_attn(const AttnArgs &a0, float *out, float *ws, size_t ws_flo
 } // namespace
 
 cudaError_t run_attn_decode(float *out, const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                            const int32_t *kpos, long long qpos, long long window, int H, int T, int D,
-                            float scale, float *ws, size_t ws_floats, int num_sms, cudaStream_t s)
+                            const int32_t *kpos, long long qpos, const int32_t *qpos_dev, long long window,
+                            int H, int T, int D, float scale, float *ws, size_t ws_floats, int num_sms,
+                            cudaStream_t s)
 {
     AttnArgs a = {};
     a.q = q;
@@ -435,6 +460,8 @@ cudaError_t run_attn_decode(float *out, const uint16_t *q, const uint16_t *k, co
     a.kpos = kpos;
     a.qpos = qpos;
     a.lo = window > 0 ? qpos - window : -1;
+    a.qpos_dev = qpos_dev;
+    a.window = window;
     a.H = H;
     a.T = T;
     a.D = D;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace w4 {
@@ -275,6 +276,17 @@ __device__ __forceinline__ void unpack_mma2(float (&c)[4], float (&d)[4], uint32
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Codes `shift` and `shift + 4` of a packed word times the step s, rounded to
+// bf16 (nearest even) and packed low-first. (code - 8) * s has at most 12
+// significant bits, so the fp32 product is exact and the rounding is the only one.
+__device__ __forceinline__ uint32_t bf16x2_of_codes(uint32_t w, int shift, float s)
+{
+    const float lo = (float)((int)((w >> shift) & 0xFu) - 8) * s;
+    const float hi = (float)((int)((w >> (shift + 4)) & 0xFu) - 8) * s;
+    __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&r);
+}
 
 // ------------------------------------------------------------- argmax ----
 

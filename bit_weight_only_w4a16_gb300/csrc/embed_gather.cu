@@ -20,14 +20,6 @@
 
 namespace w4 {
 
-__device__ __forceinline__ uint32_t bf16x2_of_codes(uint32_t w, int shift, float s)
-{
-    const float lo = (float)((int)((w >> shift) & 0xFu) - 8) * s;
-    const float hi = (float)((int)((w >> (shift + 4)) & 0xFu) - 8) * s;
-    __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&r);
-}
-
 __global__ void __launch_bounds__(256)
 embed_gather_kernel(uint16_t *__restrict__ out, const int32_t *__restrict__ ids,
                     const uint32_t *__restrict__ qt, const uint16_t *__restrict__ sc, int M,

@@ -90,9 +90,16 @@ template <int MX, int U, bool SC32, bool FULL, bool ARGMAX, bool G32, bool PAIRS
 __global__ void __launch_bounds__(512)
 gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
-               int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg)
+               int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg,
+               const int32_t *__restrict__ forced)
 {
     extern __shared__ __align__(16) unsigned char smem[];
+    if (ARGMAX && forced != nullptr && *forced >= 0) {
+        // The next token is forced: no weight is read (finalize writes it).
+        pdl_launch_dependents();
+        pdl_wait();
+        return;
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int nwarps = blockDim.x >> 5;
@@ -288,9 +295,14 @@ template <int MX, int U, int MINB, bool ARGMAX, bool G32, bool PAIRS>
 __global__ void __launch_bounds__(256, MINB)
 gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                        const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc, int N, int K,
-                       unsigned long long *__restrict__ keys, int lg)
+                       unsigned long long *__restrict__ keys, int lg, const int32_t *__restrict__ forced)
 {
     extern __shared__ __align__(16) unsigned char smem[];
+    if (ARGMAX && forced != nullptr && *forced >= 0) {
+        pdl_launch_dependents();
+        pdl_wait();
+        return;
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int nrb = (N + 15) >> 4;
@@ -734,10 +746,18 @@ gemv_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 
 __global__ void __launch_bounds__(256)
 argmax_finalize_kernel(int32_t *__restrict__ argmax, const unsigned long long *__restrict__ keys,
-                       int nblocks)
+                       int nblocks, const int32_t *__restrict__ forced)
 {
     pdl_wait();
     const int m = blockIdx.x;
+    if (forced != nullptr) {
+        const int32_t f = *forced;
+        if (f >= 0) {
+            if (threadIdx.x == 0)
+                argmax[m] = f;
+            return;
+        }
+    }
     unsigned long long k = 0ull;
     for (int i = threadIdx.x; i < nblocks; i += blockDim.x)
         k = umax64(k, keys[(size_t)m * nblocks + i]);
@@ -883,7 +903,7 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
 template <int MX, bool ARGMAX, bool PAIRS>
 static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                              const uint16_t *sc, int N, int K, unsigned long long *keys, int lg,
-                             cudaStream_t s)
+                             const int32_t *forced, cudaStream_t s)
 {
     const int Kpad = (K + kTileK - 1) / kTileK * kTileK;
     const int rbc = p.warps / p.ksplit;
@@ -911,7 +931,7 @@ static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, c
     if (e != cudaSuccess)
         return e;
     return launch_pdl(kern, dim3(p.grid), dim3(32 * p.warps), smem, s, y, x, qw, sc, N, K, p.ksplit,
-                      keys, lg);
+                      keys, lg, forced);
 }
 
 template <bool ARGMAX, bool PAIRS>
@@ -949,7 +969,7 @@ size_t decode_smem_bytes(const DecodePlan &p, int M, int K)
 template <int MX, bool ARGMAX, bool PAIRS>
 static cudaError_t launch_persist(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                                   const uint16_t *sc, int N, int K, unsigned long long *keys, int lg,
-                                  cudaStream_t s)
+                                  const int32_t *forced, cudaStream_t s)
 {
     const size_t smem = (size_t)MX * K * 2 + 16;
     auto kern = lg == 0 ? gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, true, PAIRS>
@@ -957,27 +977,27 @@ static cudaError_t launch_persist(const DecodePlan &p, float *y, const uint16_t 
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(kern, dim3(p.grid), dim3(256), smem, s, y, x, qw, sc, N, K, keys, lg);
+    return launch_pdl(kern, dim3(p.grid), dim3(256), smem, s, y, x, qw, sc, N, K, keys, lg, forced);
 }
 
 template <bool PAIRS>
 static cudaError_t dispatch_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                                    const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
-                                   bool am, cudaStream_t s)
+                                   bool am, const int32_t *fo, cudaStream_t s)
 {
     if (p.kernel == 3) {
         if (M == 1 && !PAIRS)
-            return am ? launch_persist<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, s)
-                      : launch_persist<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, s);
-        return am ? launch_persist<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, s)
-                  : launch_persist<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, s);
+            return am ? launch_persist<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, fo, s)
+                      : launch_persist<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, fo, s);
+        return am ? launch_persist<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, s)
+                  : launch_persist<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, s);
     }
     if (p.kernel == 2) {
         if (M == 1 && !PAIRS)
-            return am ? launch_m2<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, s)
-                      : launch_m2<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, s);
-        return am ? launch_m2<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, s)
-                  : launch_m2<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, s);
+            return am ? launch_m2<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, fo, s)
+                      : launch_m2<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, fo, s);
+        return am ? launch_m2<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, s)
+                  : launch_m2<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, s);
     }
     return am ? launch_m8<true, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s)
               : launch_m8<false, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s);
@@ -985,20 +1005,21 @@ static cudaError_t dispatch_decode(const DecodePlan &p, float *y, const uint16_t
 
 cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                        const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
-                       int32_t *argmax, cudaStream_t s, bool pairs)
+                       int32_t *argmax, cudaStream_t s, bool pairs, const int32_t *forced)
 {
     const bool am = argmax != nullptr;
-    cudaError_t e = pairs ? dispatch_decode<true>(p, y, x, qw, sc, M, N, K, lg, keys, am, s)
-                          : dispatch_decode<false>(p, y, x, qw, sc, M, N, K, lg, keys, am, s);
+    const int32_t *fo = am ? forced : nullptr;
+    cudaError_t e = pairs ? dispatch_decode<true>(p, y, x, qw, sc, M, N, K, lg, keys, am, fo, s)
+                          : dispatch_decode<false>(p, y, x, qw, sc, M, N, K, lg, keys, am, fo, s);
     if (e != cudaSuccess || !am)
         return e;
-    return run_argmax_finalize(argmax, keys, pairs ? M / 2 : M, p.grid, s);
+    return run_argmax_finalize(argmax, keys, pairs ? M / 2 : M, p.grid, s, fo);
 }
 
 cudaError_t run_argmax_finalize(int32_t *argmax, const unsigned long long *keys, int M, int nblocks,
-                                cudaStream_t s)
+                                cudaStream_t s, const int32_t *forced)
 {
-    return launch_pdl(argmax_finalize_kernel, dim3(M), dim3(256), 0, s, argmax, keys, nblocks);
+    return launch_pdl(argmax_finalize_kernel, dim3(M), dim3(256), 0, s, argmax, keys, nblocks, forced);
 }
 
 } // namespace w4

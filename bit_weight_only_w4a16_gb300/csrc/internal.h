@@ -35,9 +35,12 @@ size_t decode_smem_bytes(const DecodePlan &p, int M, int K);
 // lg: log2(group / 32); scales hold one step per 32 << lg codes ([N][K >> (5 + lg)]).
 // pairs: the M x-rows are M/2 (hi, lo) pairs and y has M/2 rows, each the sum of
 // its pair's products (M even; M == 2 or M <= 8 by the plan's kernel).
+// forced (argmax only, M <= 2 kernels): when *forced >= 0 as the kernels start,
+// no weight is read, y is left as it was and argmax[m] = *forced.
 cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                        const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
-                       int32_t *argmax, cudaStream_t s, bool pairs = false);
+                       int32_t *argmax, cudaStream_t s, bool pairs = false,
+                       const int32_t *forced = nullptr);
 
 // Bulk-copy streaming decode kernel (M <= 2, K % 256 == 0, 16-byte aligned
 // codes and steps): cluster size C splits K, nclusters split the row blocks.
@@ -56,9 +59,10 @@ cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const u
                        const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
                        int32_t *argmax, int *err, cudaStream_t s);
 
-// argmax[m] = index of the largest key in keys[m][0 .. nblocks).
+// argmax[m] = index of the largest key in keys[m][0 .. nblocks), or *forced
+// when forced != nullptr and *forced >= 0.
 cudaError_t run_argmax_finalize(int32_t *argmax, const unsigned long long *keys, int M, int nblocks,
-                                cudaStream_t s);
+                                cudaStream_t s, const int32_t *forced = nullptr);
 
 cudaError_t run_embed_gather(uint16_t *out, const int32_t *ids, const uint32_t *qt,
                              const uint16_t *sc, int M, int N, int K, int lg, int32_t *status,
@@ -87,10 +91,30 @@ cudaError_t run_prefill(const PrefillPlan &p, float *y, const uint16_t *x, const
 // Sylvester-Hadamard matrix with blocks of b (a power of two dividing K), fp32.
 cudaError_t run_hadamard_split(uint16_t *x2, const uint16_t *x, int M, int K, int b, cudaStream_t s);
 
+// Launches a kernel whose bounded mbarrier wait cannot complete: it gives up
+// within ~1 ms and sets bit 2 of *err.
+cudaError_t run_bounded_wait_selftest(int *err, cudaStream_t s);
+
 // Decode attention of one query token (H <= 8 query heads sharing one key/value
 // head, D in {128, 256, 384, 512}) over T cache slots; split partials in ws.
+// With qpos_dev != nullptr the query position is *qpos_dev, read at run time.
 cudaError_t run_attn_decode(float *out, const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                            const int32_t *kpos, long long qpos, long long window, int H, int T, int D,
-                            float scale, float *ws, size_t ws_floats, int num_sms, cudaStream_t s);
+                            const int32_t *kpos, long long qpos, const int32_t *qpos_dev, long long window,
+                            int H, int T, int D, float scale, float *ws, size_t ws_floats, int num_sms,
+                            cudaStream_t s);
+
+// Writes the new token's key and value rows into slot (*pos mod T) of a ring
+// (kpos != nullptr, which records *pos there) or slot *pos of a full cache;
+// a position outside the cache sets *status = 1 and writes nothing.
+cudaError_t run_kv_append(uint16_t *kc, uint16_t *vc, int32_t *kpos, const uint16_t *kn, const uint16_t *vn,
+                          int32_t *pos, int T, int D, int32_t *status, cudaStream_t s);
+
+// Next-step prologue: tok = argmax[0]; tokens[*pos + 1] = tok (when inside
+// [0, cap)); *pos += 1; x_next = the bf16 row tok of the 4-bit table. A token
+// outside [0, V) gives a zero row and sets status bit 0; a full history sets
+// bit 1.
+cudaError_t run_decode_prologue(uint16_t *x_next, int32_t *tokens, int32_t *pos, const int32_t *argmax,
+                                const uint32_t *qt, const uint16_t *sc, int V, int K, int lg, int cap,
+                                int32_t *status, cudaStream_t s);
 
 } // namespace w4

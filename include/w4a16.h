@@ -67,11 +67,21 @@ int w4_init(void);
 
 /*
  * Reads and clears the device error word of the current device after a
- * cudaDeviceSynchronize. *code is 0 when every kernel finished normally; bit 0
- * means a kernel's bounded wait on its own shared-memory pipeline ran out (the
- * kernel then returned without hanging, and its outputs are not valid).
+ * cudaDeviceSynchronize. *code is 0 when every kernel finished normally. A set
+ * bit means that a kernel's bounded wait on its own shared-memory pipeline ran
+ * out: bit 0 the streaming decode kernel, bit 1 the prefill GEMM, bit 2 the
+ * self-test below. That kernel then returned without hanging; its outputs are
+ * not valid, and the context stays usable.
  */
 int w4_device_error(int32_t *code);
+
+/*
+ * Self-test of the failure path: launches one kernel on `stream` whose bounded
+ * wait on an mbarrier that nothing arrives at gives up (after at most ~1 ms)
+ * and sets bit 2 of the device error word, exactly as a kernel whose pipeline
+ * stalled sets its bit and returns. Returns W4_OK when the launch succeeded.
+ */
+int w4_selftest_wait_timeout(void *stream);
 
 /*
  * W4A16 matrix-vector product for decode, M in [1, 8].
@@ -200,6 +210,79 @@ int w4a16_gemv_hadamard(float *y, int32_t *argmax, const uint16_t *x, const uint
 int w4_attn_decode(float *out, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                    const int32_t *kpos, int qpos, int window, int H, int T, int D, float scale,
                    void *stream);
+
+/*
+ * Decode attention with the query position in device memory (source: "Gemma 4
+ * E2B on a 4 GB GPU with pure PyTorch", CUDA-graph paragraph: a cache length
+ * held as a host integer is frozen into a captured graph, so the engine keeps
+ * every position on the GPU). Same operation, arguments, limits and errors as
+ * w4_attn_decode, except that the query position is *qpos (int32, 4-byte
+ * aligned), read when the kernels run, and `window` derives the lower bound
+ * from it; one captured call serves every decode step.
+ */
+int w4_attn_decode_devpos(float *out, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const int32_t *kpos, const int32_t *qpos, int window, int H, int T, int D,
+                          float scale, void *stream);
+
+/*
+ * Appends the new token's key and value rows to a one-head cache at the device
+ * position *pos (source: the same article's cache paragraph: full layers keep
+ * one slot per position, sliding layers a ring of slots that records each
+ * slot's position).
+ *
+ *   kpos != NULL (ring of T slots): slot = *pos mod T, kpos[slot] = *pos
+ *   kpos == NULL (full cache):      slot = *pos, which must lie in [0, T)
+ *   k_cache[slot][:] = k_new, v_cache[slot][:] = v_new (bf16 [D] each)
+ *
+ * k_cache, v_cache bf16 [T][D]; k_new, v_new bf16 [D]; all 16-byte aligned;
+ * pos, kpos, status int32, 4-byte aligned. D a multiple of 8, T * D < 2^31. A
+ * negative position, or one outside a full cache, writes nothing and sets
+ * *status = 1 (status may be NULL). *pos is read when the kernel runs and is
+ * not changed.
+ */
+int w4_kv_append(uint16_t *k_cache, uint16_t *v_cache, int32_t *kpos, const uint16_t *k_new,
+                 const uint16_t *v_new, const int32_t *pos, int T, int D, int32_t *status, void *stream);
+
+/*
+ * Greedy LM head with a forced-token skip (source: "Gemma 4 E2B on a 4 GB GPU
+ * with pure PyTorch", tool-calling paragraph: when the constrained decoder
+ * admits exactly one token, the step skips the int4 LM-head read).
+ *
+ *   *forced <  0: as w4a16_gemv_argmax with M = 1 (y = x W^T, argmax[0] = the
+ *                 lowest index of the maximum)
+ *   *forced >= 0: no weight is read, y is left as it was, argmax[0] = *forced
+ *
+ * forced: device int32 (4-byte aligned). The decode kernel reads it when it
+ * starts, before it waits on the kernel preceding it on the stream (its weight
+ * loads begin at launch), so *forced must hold this step's value before that
+ * preceding kernel starts: write it with a copy issued ahead of the step's
+ * kernels, as a host-side constrained decoder does, not from the kernel right
+ * before this call. Arguments and errors otherwise as w4a16_gemv_argmax.
+ */
+int w4a16_gemv_argmax_forced(float *y, int32_t *argmax, const uint16_t *x, const uint32_t *qweight,
+                             const uint16_t *scales, int N, int K, int group, const int32_t *forced,
+                             void *stream);
+
+/*
+ * Next-step prologue of a device-resident decode loop (source: "Gemma 4 E2B on
+ * a 4 GB GPU with pure PyTorch": the CUDA-graph paragraph, with every position
+ * on the GPU; the emb4 paragraph, in which the embedding and the LM head share
+ * one 4-bit table; Step 2, in which the row lookup happens on the card).
+ *
+ *   tok = *token                      (the LM head's argmax, or the forced token)
+ *   tokens[*pos + 1] = tok            (when tokens != NULL and *pos + 1 in [0, cap))
+ *   *pos = *pos + 1
+ *   x_next[k] = bf16_rne((code(tok, k) - 8) * scale(tok, k/group))  (as w4_embed_gather)
+ *
+ * qtable uint32 [V][K/8], scales bf16 [V][K/group] (the 4-bit table, group 32,
+ * 64, 128, 256 or 512); x_next bf16 [K] (16-byte aligned); pos, token, tokens,
+ * status int32 (4-byte aligned). A token outside [0, V) gives a zero row and
+ * sets bit 0 of *status; a full history sets bit 1 (status may be NULL; bits
+ * are only ever set). The position is read and written when the kernel runs.
+ */
+int w4_decode_prologue(uint16_t *x_next, int32_t *tokens, int32_t *pos, const int32_t *token,
+                       const uint32_t *qtable, const uint16_t *scales, int V, int K, int group, int cap,
+                       int32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

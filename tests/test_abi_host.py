@@ -100,6 +100,28 @@ def test_validation_before_any_launch(lib):
     assert l.w4_attn_decode(A, A, _addr((1 << 20) + 8), A, None, 0, 0, 8, 16, 512, f, None) == 3
     assert l.w4_attn_decode(A, A, A, A, _addr((1 << 20) + 2), 0, 0, 8, 16, 512, f, None) == 3
     assert l.w4_attn_decode(A, A, A, A, None, 0, 0, 8, 1 << 22, 512, f, None) == 1
+    # attention at a device position: the same checks plus the position pointer
+    assert l.w4_attn_decode_devpos(A, A, A, A, None, None, 0, 8, 16, 512, f, None) == 1
+    assert l.w4_attn_decode_devpos(A, A, A, A, None, A, 0, 9, 16, 512, f, None) == 2
+    assert l.w4_attn_decode_devpos(A, A, A, A, None, _addr((1 << 20) + 2), 0, 8, 16, 512, f, None) == 3
+    # key/value append: NULL, width, alignment
+    assert l.w4_kv_append(A, A, None, A, A, None, 16, 512, None, None) == 1
+    assert l.w4_kv_append(A, A, None, A, A, A, 16, 100, None, None) == 1
+    assert l.w4_kv_append(A, A, None, A, A, A, 0, 512, None, None) == 1
+    assert l.w4_kv_append(A, A, None, _addr((1 << 20) + 8), A, A, 16, 512, None, None) == 3
+    assert l.w4_kv_append(A, A, _addr((1 << 20) + 2), A, A, A, 16, 512, None, None) == 3
+    # forced-token LM head: NULL forced, group, alignment
+    assert l.w4a16_gemv_argmax_forced(A, A, A, A, A, 16, 64, 32, None, None) == 1
+    assert l.w4a16_gemv_argmax_forced(A, None, A, A, A, 16, 64, 32, A, None) == 1
+    assert l.w4a16_gemv_argmax_forced(A, A, A, A, A, 16, 96, 48, A, None) == 2
+    assert l.w4a16_gemv_argmax_forced(A, A, A, A, A, 16, 64, 32, _addr((1 << 20) + 2), None) == 3
+    # prologue: NULL, sizes, group, history capacity, alignment
+    assert l.w4_decode_prologue(A, None, A, None, A, A, 16, 64, 32, 0, None, None) == 1
+    assert l.w4_decode_prologue(A, None, A, A, A, A, 0, 64, 32, 0, None, None) == 1
+    assert l.w4_decode_prologue(A, A, A, A, A, A, 16, 64, 32, 0, None, None) == 1
+    assert l.w4_decode_prologue(A, None, A, A, A, A, 16, 96, 48, 0, None, None) == 2
+    assert l.w4_decode_prologue(A, None, A, A, A, A, 16, 96, 64, 0, None, None) == 1
+    assert l.w4_decode_prologue(_addr((1 << 20) + 8), None, A, A, A, A, 16, 64, 32, 0, None, None) == 3
 
 
 def test_no_device_reported_without_gpu(lib):
