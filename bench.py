@@ -641,20 +641,27 @@ def run_ours(args, rank, world):
             e2e_step()
         torch.cuda.synchronize()
         barrier()
-        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # Three timed blocks; the median block is reported (the host link is
+        # shared with other jobs on the machine, and one block of ~50 ms can
+        # catch a burst of their traffic), every block's time beside it.
         e2e_steps = max(2, min(args.steps, 10))
-        q0.record(stream)
-        for cs in cstreams:
-            cs.wait_stream(stream)  # every copy of the timed steps starts after q0
-        for _ in range(e2e_steps):
-            e2e_step()
-        for cs in cstreams:
-            stream.wait_stream(cs)
-        q1.record(stream)
-        torch.cuda.synchronize()
-        te = max_over_ranks(q0.elapsed_time(q1) / e2e_steps, world, dev)
+        blocks = []
+        for _ in range(3):
+            q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            q0.record(stream)
+            for cs in cstreams:
+                cs.wait_stream(stream)  # every copy of the timed steps starts after q0
+            for _ in range(e2e_steps):
+                e2e_step()
+            for cs in cstreams:
+                stream.wait_stream(cs)
+            q1.record(stream)
+            torch.cuda.synchronize()
+            blocks.append(max_over_ranks(q0.elapsed_time(q1) / e2e_steps, world, dev))
+        te = sorted(blocks)[1]
         e2e = {"value": job_rate(te, nbytes, world), "unit": "GB/s", "ms_per_step": te,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "blocks_ms_per_step": blocks, "steps_per_block": e2e_steps}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
