@@ -325,66 +325,64 @@ attn_split_kernel(const AttnArgs a)
 }
 
 // out[h][d] = sum_s O_s[h][d] 2^(m_s - m) / sum_s l_s 2^(m_s - m) with m the
-// largest m_s. Block (32 dims, head): warp w adds the slices s = w mod 8 for
-// its lane's dim, then the 8 warp sums are added in warp order; the slice
-// factors and the normaliser come from fixed-shape reductions (deterministic).
+// largest m_s. Block (32 dims, head), one pass: warp w merges the slices
+// s = w, w + 8, ... in that order into a running (max, sum, output) for its
+// lane's dim, four slices' loads in flight at a time; warp 0 then merges the 8
+// warp states in warp order (deterministic). A slice that kept no slot
+// (m_s = -inf) adds nothing.
 constexpr int kCombWarps = 8;
+constexpr int kCombBatch = 4;
+
+__device__ __forceinline__ void merge_state(float &M, float &L, float &O, float m, float l, float o)
+{
+    if (m == -INFINITY)
+        return;
+    const float Mn = fmaxf(M, m);
+    const float a = exp2f(M - Mn); // 0 while nothing was merged (M = -inf)
+    const float b = exp2f(m - Mn);
+    L = fmaf(L, a, l * b);
+    O = fmaf(O, a, o * b);
+    M = Mn;
+}
 
 __global__ void __launch_bounds__(kCombWarps * 32)
 attn_combine_kernel(float *__restrict__ out, const float *__restrict__ ws_o, const float *__restrict__ ws_ml,
                     int nsplit, int D)
 {
-    extern __shared__ float fac[]; // [nsplit] slice factors
-    __shared__ float red[kCombWarps * 32];
-    __shared__ float part[kCombWarps][32];
+    __shared__ float sm[kCombWarps], sl[kCombWarps], so[kCombWarps][32];
     pdl_wait();
     const int h = blockIdx.y, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int d = blockIdx.x * 32 + lane;
-    const int nt = blockDim.x;
+    const bool dok = d < D;
 
-    float mx = -INFINITY;
-    for (int s = threadIdx.x; s < nsplit; s += nt)
-        mx = fmaxf(mx, ws_ml[((size_t)s * kHeads + h) * 2]);
-    red[threadIdx.x] = mx;
-    __syncthreads();
-    for (int o = nt / 2; o > 0; o >>= 1) {
-        if (threadIdx.x < o)
-            red[threadIdx.x] = fmaxf(red[threadIdx.x], red[threadIdx.x + o]);
-        __syncthreads();
+    float M = -INFINITY, L = 0.f, O = 0.f;
+    for (int s0 = w; s0 < nsplit; s0 += kCombBatch * kCombWarps) {
+        float mv[kCombBatch], lv[kCombBatch], ov[kCombBatch];
+#pragma unroll
+        for (int j = 0; j < kCombBatch; ++j) {
+            const int sidx = s0 + j * kCombWarps;
+            const bool ok = sidx < nsplit;
+            const size_t r = (size_t)(ok ? sidx : 0) * kHeads + h;
+            mv[j] = ok ? ws_ml[r * 2] : -INFINITY;
+            lv[j] = ok ? ws_ml[r * 2 + 1] : 0.f;
+            ov[j] = (ok && dok) ? ws_o[r * D + d] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < kCombBatch; ++j)
+            merge_state(M, L, O, mv[j], lv[j], ov[j]);
     }
-    const float mstar = red[0];
-    __syncthreads();
-
-    float ls = 0.f;
-    for (int s = threadIdx.x; s < nsplit; s += nt) {
-        const float m = ws_ml[((size_t)s * kHeads + h) * 2];
-        const float f = (m == -INFINITY) ? 0.f : exp2f(m - mstar);
-        fac[s] = f;
-        ls = fmaf(ws_ml[((size_t)s * kHeads + h) * 2 + 1], f, ls);
+    if (lane == 0) {
+        sm[w] = M;
+        sl[w] = L;
     }
-    red[threadIdx.x] = ls;
+    so[w][lane] = O;
     __syncthreads();
-    for (int o = nt / 2; o > 0; o >>= 1) {
-        if (threadIdx.x < o)
-            red[threadIdx.x] += red[threadIdx.x + o];
-        __syncthreads();
-    }
-    const float L = red[0];
-
-    float acc = 0.f;
-    if (d < D) {
-#pragma unroll 4
-        for (int s = w; s < nsplit; s += kCombWarps)
-            acc = fmaf(ws_o[((size_t)s * kHeads + h) * D + d], fac[s], acc);
-    }
-    part[w][lane] = acc;
-    __syncthreads();
-    if (w == 0 && d < D) {
-        float O = 0.f;
+    if (w == 0 && dok) {
+        float Mt = -INFINITY, Lt = 0.f, Ot = 0.f;
 #pragma unroll
         for (int u = 0; u < kCombWarps; ++u)
-            O += part[u][lane];
-        out[(size_t)h * D + d] = (mstar != -INFINITY && L > 0.f) ? O / L : 0.f;
+            merge_state(Mt, Lt, Ot, sm[u], sl[u], so[u][lane]);
+        out[(size_t)h * D + d] = (Mt != -INFINITY && Lt > 0.f) ? Ot / Lt : 0.f;
     }
 }
 
@@ -438,7 +436,7 @@ cudaError_t launch_attn(const AttnArgs &a0, float *out, float *ws, size_t ws_flo
     cudaLaunchConfig_t cfg2 = {};
     cfg2.gridDim = dim3(a0.D / 32, a0.H);
     cfg2.blockDim = dim3(kCombWarps * 32);
-    cfg2.dynamicSmemBytes = (size_t)nsplit * sizeof(float);
+    cfg2.dynamicSmemBytes = 0;
     cfg2.stream = s;
     cfg2.attrs = attr;
     cfg2.numAttrs = 1;
