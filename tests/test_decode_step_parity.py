@@ -101,9 +101,9 @@ def test_masked_tail_of_full_cache_is_never_read(w4):
 
 # ---------------------------------------------------------------- append ----
 
-def test_kv_append_ring_and_full_cache(w4):
+@pytest.mark.parametrize("T,D,P", [(16, 128, 41), (5, 72, 13)])
+def test_kv_append_ring_and_full_cache(w4, T, D, P):
     import torch
-    T, D, P = 16, 128, 41
     kall, vall = synth.gen_attn_kv(940, P, D)
     kr = torch.zeros((T, D), dtype=torch.int16, device="cuda")
     vr = torch.zeros_like(kr)
@@ -130,6 +130,7 @@ def test_kv_append_ring_and_full_cache(w4):
         assert int(status.item()) == sto  # the full cache overflows from position 16 on
         status.zero_()
     assert int(pos.item()) == P - 1  # the append never moves the position
+    status.zero_()
     pos.fill_(-3)
     before = bits16(kr).copy()
     w4.w4_kv_append(kr, vr, kd[0], vd[0], pos, kpos=kp, status=status)
@@ -171,9 +172,10 @@ def test_forced_lm_head(w4, N, K, group):
 
 # -------------------------------------------------------------- prologue ----
 
-def test_prologue_bit_exact(w4):
+@pytest.mark.parametrize("group", [64, 512])
+def test_prologue_bit_exact(w4, group):
     import torch
-    V, K, group = 1000, 1536, 64
+    V, K = 1000, 1536
     qt = synth.gen_qweight(960, V, K)
     sc = synth.gen_scales(960, V, K, group)
     qd, sd = to_dev_u32(qt), to_dev_bits16(sc)
@@ -205,11 +207,13 @@ def test_prologue_bit_exact(w4):
 
 # ------------------------------------------------- graph-replayed loop ----
 
-def test_graph_replayed_decode_loop(w4):
+@pytest.mark.parametrize("tied", [False, True])
+def test_graph_replayed_decode_loop(w4, tied):
     """150 decode steps replayed from ONE captured graph: append (ring of 64 slots
     and a full cache), attention at the device position for both, the LM head
     (every third token forced), prologue. Positions, history and x never leave
-    the device; per-step host work is two row copies and the forced token."""
+    the device; per-step host work is two row copies and the forced token.
+    tied: the embedding and the LM head are one table (the emb4 paragraph)."""
     import torch
     S, H, D, Tr, Tf = 150, 8, 256, 64, 256
     V, K, group = 4096, 1536, 64
@@ -217,13 +221,14 @@ def test_graph_replayed_decode_loop(w4):
     q = synth.gen_attn_q(970, H, D)
     kall, vall = synth.gen_attn_kv(971, S, D)
     eq, es = synth.gen_qweight(972, V, K), synth.gen_scales(972, V, K, group)
-    hq, hs = synth.gen_qweight(973, V, K), synth.gen_scales(973, V, K, group)
+    hq, hs = (eq, es) if tied else (synth.gen_qweight(973, V, K), synth.gen_scales(973, V, K, group))
     forced_seq = np.array([(s * 7919) % V if s % 3 == 1 else -1 for s in range(S)], np.int32)
     start = 17
 
     dev = torch.device("cuda")
     qd, kall_d, vall_d = to_dev_bits16(q), to_dev_bits16(kall), to_dev_bits16(vall)
-    eqd, esd, hqd, hsd = to_dev_u32(eq), to_dev_bits16(es), to_dev_u32(hq), to_dev_bits16(hs)
+    eqd, esd = to_dev_u32(eq), to_dev_bits16(es)
+    hqd, hsd = (eqd, esd) if tied else (to_dev_u32(hq), to_dev_bits16(hs))
     forced_d = torch.from_numpy(forced_seq).to(dev)
     kr = torch.zeros((Tr, D), dtype=torch.int16, device=dev)
     vr = torch.zeros_like(kr)
