@@ -413,8 +413,8 @@ int w4_kv_append(uint16_t *k_cache, uint16_t *v_cache, int32_t *kpos, const uint
     int rc = device_state(&st);
     if (rc != W4_OK)
         return rc;
-    cudaError_t e = w4::run_kv_append(k_cache, v_cache, kpos, k_new, v_new, const_cast<int32_t *>(pos), T, D,
-                                      status, static_cast<cudaStream_t>(stream));
+    cudaError_t e = w4::run_kv_append(k_cache, v_cache, kpos, k_new, v_new, pos, T, D, status,
+                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? W4_OK : cuda_fail(e);
 }
 

@@ -102,11 +102,11 @@ cudaLaunchConfig_t one_cta(unsigned threads, cudaStream_t s, cudaLaunchAttribute
 } // namespace
 
 cudaError_t run_kv_append(uint16_t *kc, uint16_t *vc, int32_t *kpos, const uint16_t *kn, const uint16_t *vn,
-                          int32_t *pos, int T, int D, int32_t *status, cudaStream_t s)
+                          const int32_t *pos, int T, int D, int32_t *status, cudaStream_t s)
 {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = one_cta(128, s, attr);
-    return cudaLaunchKernelEx(&cfg, kv_append_kernel, kc, vc, kpos, kn, vn, (const int32_t *)pos, T, D, status);
+    return cudaLaunchKernelEx(&cfg, kv_append_kernel, kc, vc, kpos, kn, vn, pos, T, D, status);
 }
 
 cudaError_t run_decode_prologue(uint16_t *x_next, int32_t *tokens, int32_t *pos, const int32_t *argmax,

@@ -107,7 +107,7 @@ cudaError_t run_attn_decode(float *out, const uint16_t *q, const uint16_t *k, co
 // (kpos != nullptr, which records *pos there) or slot *pos of a full cache;
 // a position outside the cache sets *status = 1 and writes nothing.
 cudaError_t run_kv_append(uint16_t *kc, uint16_t *vc, int32_t *kpos, const uint16_t *kn, const uint16_t *vn,
-                          int32_t *pos, int T, int D, int32_t *status, cudaStream_t s);
+                          const int32_t *pos, int T, int D, int32_t *status, cudaStream_t s);
 
 // Next-step prologue: tok = argmax[0]; tokens[*pos + 1] = tok (when inside
 // [0, cap)); *pos += 1; x_next = the bf16 row tok of the 4-bit table. A token
