@@ -321,6 +321,10 @@ def measure_rows(w4, dev, stream, sweep=None):
     us = graph_time(lambda: [w4.w4a16_gemv(x, q, sc, out=y, stream=stream) for q in qs]) / copies
     b = stage_bytes(N, K)
     res["gemv_2048x2048_m1"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    # The same with Hadamard-rotated weights (blocks of 256): x H formed by the
+    # decode kernel while it stages x.
+    us = graph_time(lambda: [w4.w4a16_gemv_hadamard(x, q, sc, 256, out=y, stream=stream) for q in qs]) / copies
+    res["gemv_hadamard_2048x2048_b256"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
     del qs
 
     # Vocabulary projection 262144x1536 with the fused argmax (226 MB).
@@ -362,6 +366,15 @@ def measure_rows(w4, dev, stream, sweep=None):
         b = sum(stage_bytes(qq.shape[0], xx.shape[1]) for (xx, qq, ss, yy) in calls)
         res["sweep_unfused_245"] = {"us": us, "ms": us / 1e3, "GBps": b / us / 1e3, "bytes": b,
                                     "calls": len(calls)}
+
+        # Every call of the sweep with Hadamard-rotated weights (blocks of 512,
+        # as a model whose linear weights are all rotated would run).
+        def rotated():
+            for st in sweep.stages:
+                w4.w4a16_gemv_hadamard(st["x"], st["qw"], st["sc"], 512, out=st["y"], stream=stream)
+        us = graph_time(rotated, reps=10)
+        b = sweep_bytes()
+        res["sweep_hadamard_b512"] = {"us": us, "ms": us / 1e3, "GBps": b / us / 1e3, "bytes": b}
 
     # The LM head as the fastgemma card stores it: Hadamard-rotated, group 256,
     # with the activation's transform (blocks of 512) and the greedy pick.

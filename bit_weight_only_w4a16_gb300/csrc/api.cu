@@ -355,13 +355,23 @@ int w4a16_gemv_hadamard(float *y, int32_t *argmax, const uint16_t *x, const uint
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // One x-row, blocks of 256 or 512, K % 128 == 0: the decode kernel forms
+    // x H itself while staging x (no transform launch, no scratch rows).
+    if (M == 1 && (hblock == 256 || hblock == 512) && K % 128 == 0) {
+        const w4::DecodePlan p = w4::plan_decode(2, N, K, st->num_sms);
+        if (p.kernel != 8 && decode_fits(p, 2, K) && (!argmax || (size_t)p.grid <= kKeyCapacity)) {
+            cudaError_t e = w4::run_decode(p, y, x, qweight, scales, 2, N, K, w4::group_shift(group),
+                                           argmax ? st->keys : nullptr, argmax, s, true, nullptr, hblock);
+            return e == cudaSuccess ? W4_OK : cuda_fail(e);
+        }
+    }
     // The rotated activation's (hi, lo) rows live in the split scratch.
     if ((size_t)2 * M * K * sizeof(uint16_t) > kWsFloats * sizeof(float))
         return W4_ERR_UNSUPPORTED;
     const w4::DecodePlan p = w4::plan_decode(2 * M, N, K, st->num_sms);
     if (!decode_fits(p, 2 * M, K) || (argmax && (size_t)M * p.grid > kKeyCapacity))
         return W4_ERR_UNSUPPORTED;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint16_t *x2 = reinterpret_cast<uint16_t *>(st->ws);
     cudaError_t e = w4::run_hadamard_split(x2, x, M, K, hblock, s);
     if (e == cudaSuccess)

@@ -101,6 +101,84 @@ __device__ __forceinline__ void stage_x_rows_async(uint4 *xs, const uint16_t *x,
         xs[i] = permute_x8(xs[i]);
 }
 
+// Fused rotation for the Hadamard-rotated GEMV at M = 1 (blocks of b = 32 * PL
+// values, PL = 8 or 16, K % 128 == 0): x-rows 0, 1 of xs become hi = bf16(v),
+// lo = bf16(v - hi) of v = (x H)[k], permuted as stage_x_rows lays them out.
+// Warp w transforms blocks w, w + nwarps, ...: lane l holds values
+// [PL*l, PL*l + PL) of the block in registers, so the butterfly stages over
+// the low log2(PL) index bits stay in the lane and the next 5 are lane-bit
+// exchanges (shfl_xor). Stage order and pairing (p + q, p - q) are those of
+// the standalone transform kernel, so both paths give the same bits. All of a
+// warp's x loads are issued before its first stage.
+template <int PL>
+__device__ __forceinline__ void stage_x_hadamard(uint4 *xs, const uint16_t *x, int K, int cpr, float norm)
+{
+    constexpr int B = 32 * PL, NC = PL / 8; // values and 8-value chunks per lane
+    constexpr int kMaxBlk = 1;             // blocks a warp keeps in flight
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int blk0 = threadIdx.x >> 5; blk0 * B < K; blk0 += kMaxBlk * nw) {
+        uint4 raw[kMaxBlk][NC];
+#pragma unroll
+        for (int q = 0; q < kMaxBlk; ++q) {
+            const int blk = blk0 + q * nw;
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+                raw[q][c] = blk * B < K ? *reinterpret_cast<const uint4 *>(x + blk * B + lane * PL + 8 * c)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < kMaxBlk; ++q) {
+            const int blk = blk0 + q * nw;
+            if (blk * B >= K)
+                break;
+            float v[PL];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                const uint32_t u[4] = {raw[q][c].x, raw[q][c].y, raw[q][c].z, raw[q][c].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[8 * c + 2 * j] = bf16lo_to_f32(u[j]);
+                    v[8 * c + 2 * j + 1] = bf16hi_to_f32(u[j]);
+                }
+            }
+#pragma unroll
+            for (int h = 1; h < PL; h <<= 1)
+#pragma unroll
+                for (int r = 0; r < PL; ++r)
+                    if (!(r & h)) {
+                        const float pv = v[r], qv = v[r + h];
+                        v[r] = pv + qv;
+                        v[r + h] = pv - qv;
+                    }
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int r = 0; r < PL; ++r) {
+                    const float o = __shfl_xor_sync(0xFFFFFFFFu, v[r], m);
+                    v[r] = upper ? o - v[r] : v[r] + o;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float r0 = v[8 * c + 2 * j] * norm, r1 = v[8 * c + 2 * j + 1] * norm;
+                    const __nv_bfloat16 h0 = __float2bfloat16_rn(r0), h1 = __float2bfloat16_rn(r1);
+                    const __nv_bfloat16 l0 = __float2bfloat16_rn(r0 - __bfloat162float(h0));
+                    const __nv_bfloat16 l1 = __float2bfloat16_rn(r1 - __bfloat162float(h1));
+                    hw[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                    lw[j] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                }
+                const int cc = ((blk * B + lane * PL) >> 3) + c;
+                xs[cc] = permute_x8(make_uint4(hw[0], hw[1], hw[2], hw[3]));
+                xs[cpr + cc] = permute_x8(make_uint4(lw[0], lw[1], lw[2], lw[3]));
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- m2 ----
 
 // FULL (K % 128 == 0, implies SC32): every k-tile is whole, so the loads need
@@ -113,7 +191,7 @@ __global__ void __launch_bounds__(512)
 gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
                int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg,
-               const int32_t *__restrict__ forced)
+               const int32_t *__restrict__ forced, int hb, float hnorm)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     if (ARGMAX && forced != nullptr && *forced >= 0) {
@@ -185,8 +263,10 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     };
 
     // Stream the first weight tiles before waiting on the previous kernel.
+    // (hb > 0: x is one row that this kernel rotates into the pair rows.)
+    const bool fused = PAIRS && hb > 0;
     if (threadIdx.x == 32)
-        prefetch_l2_bulk(x, (uint32_t)(MX * K * 2));
+        prefetch_l2_bulk(x, (uint32_t)((fused ? 1 : MX) * K * 2));
 #pragma unroll
     for (int u = 0; u < U; ++u)
         if (u < nkt)
@@ -197,8 +277,15 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
     // Stage x, permuted into the B-operand pair order, and a zero chunk.
     uint4 *xs = reinterpret_cast<uint4 *>(smem);
     const int chunks_per_row = Kpad >> 3;
-    stage_x_rows(xs, x, MX, K, chunks_per_row);
     uint4 *zero_chunk = xs + MX * chunks_per_row;
+    if (fused) {
+        if (hb == 256)
+            stage_x_hadamard<8>(xs, x, K, chunks_per_row, hnorm);
+        else
+            stage_x_hadamard<16>(xs, x, K, chunks_per_row, hnorm);
+    } else {
+        stage_x_rows(xs, x, MX, K, chunks_per_row);
+    }
     if (threadIdx.x == 0)
         *zero_chunk = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
@@ -322,7 +409,8 @@ template <int MX, int U, int MINB, bool ARGMAX, bool G32, bool PAIRS>
 __global__ void __launch_bounds__(256, MINB)
 gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                        const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc, int N, int K,
-                       unsigned long long *__restrict__ keys, int lg, const int32_t *__restrict__ forced)
+                       unsigned long long *__restrict__ keys, int lg, const int32_t *__restrict__ forced,
+                       int hb, float hnorm)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     if (ARGMAX && forced != nullptr && *forced >= 0) {
@@ -368,8 +456,9 @@ gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         }
     };
 
+    const bool fused = PAIRS && hb > 0; // x is one row, rotated here into the pair rows
     if (threadIdx.x == 32)
-        prefetch_l2_bulk(x, (uint32_t)(MX * K * 2));
+        prefetch_l2_bulk(x, (uint32_t)((fused ? 1 : MX) * K * 2));
 #pragma unroll
     for (int u = 0; u < U; ++u)
         if (u < Q)
@@ -379,8 +468,15 @@ gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 
     uint4 *xs = reinterpret_cast<uint4 *>(smem);
     const int chunks_per_row = K >> 3;
-    stage_x_rows(xs, x, MX, K, chunks_per_row);
     uint4 *zero_chunk = xs + MX * chunks_per_row;
+    if (fused) {
+        if (hb == 256)
+            stage_x_hadamard<8>(xs, x, K, chunks_per_row, hnorm);
+        else
+            stage_x_hadamard<16>(xs, x, K, chunks_per_row, hnorm);
+    } else {
+        stage_x_rows(xs, x, MX, K, chunks_per_row);
+    }
     constexpr int MO = PAIRS ? MX / 2 : MX; // output rows (PAIRS: x-rows 0, 1 are one)
     __shared__ unsigned long long ck[MO];
     if (threadIdx.x == 0)
@@ -960,13 +1056,14 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
 template <int MX, bool ARGMAX, bool PAIRS>
 static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                              const uint16_t *sc, int N, int K, unsigned long long *keys, int lg,
-                             const int32_t *forced, cudaStream_t s)
+                             const int32_t *forced, int hb, cudaStream_t s)
 {
     const int Kpad = (K + kTileK - 1) / kTileK * kTileK;
     const int rbc = p.warps / p.ksplit;
     size_t smem = (size_t)MX * Kpad * 2 + 16;
     if (p.ksplit > 1)
         smem += (size_t)rbc * p.ksplit * MX * 16 * sizeof(float);
+
     const bool sc32 = (K % 64) == 0, full = (K % kTileK) == 0;
     // Groups above 32 take the same kernels with a run-time step shift.
     auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, false, ARGMAX, true, PAIRS>
@@ -988,7 +1085,7 @@ static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, c
     if (e != cudaSuccess)
         return e;
     return launch_pdl(kern, dim3(p.grid), dim3(32 * p.warps), smem, s, y, x, qw, sc, N, K, p.ksplit,
-                      keys, lg, forced);
+                      keys, lg, forced, hb, hb > 0 ? 1.0f / sqrtf((float)hb) : 0.f);
 }
 
 template <bool ARGMAX, bool PAIRS>
@@ -1026,7 +1123,7 @@ size_t decode_smem_bytes(const DecodePlan &p, int M, int K)
 template <int MX, bool ARGMAX, bool PAIRS>
 static cudaError_t launch_persist(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                                   const uint16_t *sc, int N, int K, unsigned long long *keys, int lg,
-                                  const int32_t *forced, cudaStream_t s)
+                                  const int32_t *forced, int hb, cudaStream_t s)
 {
     const size_t smem = (size_t)MX * K * 2 + 16;
     auto kern = lg == 0 ? gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, true, PAIRS>
@@ -1034,27 +1131,28 @@ static cudaError_t launch_persist(const DecodePlan &p, float *y, const uint16_t 
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
-    return launch_pdl(kern, dim3(p.grid), dim3(256), smem, s, y, x, qw, sc, N, K, keys, lg, forced);
+    return launch_pdl(kern, dim3(p.grid), dim3(256), smem, s, y, x, qw, sc, N, K, keys, lg, forced, hb,
+                      hb > 0 ? 1.0f / sqrtf((float)hb) : 0.f);
 }
 
 template <bool PAIRS>
 static cudaError_t dispatch_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                                    const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
-                                   bool am, const int32_t *fo, cudaStream_t s)
+                                   bool am, const int32_t *fo, int hb, cudaStream_t s)
 {
     if (p.kernel == 3) {
         if (M == 1 && !PAIRS)
-            return am ? launch_persist<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, fo, s)
-                      : launch_persist<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, fo, s);
-        return am ? launch_persist<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, s)
-                  : launch_persist<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, s);
+            return am ? launch_persist<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s)
+                      : launch_persist<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s);
+        return am ? launch_persist<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s)
+                  : launch_persist<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s);
     }
     if (p.kernel == 2) {
         if (M == 1 && !PAIRS)
-            return am ? launch_m2<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, fo, s)
-                      : launch_m2<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, fo, s);
-        return am ? launch_m2<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, s)
-                  : launch_m2<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, s);
+            return am ? launch_m2<1, true, false>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s)
+                      : launch_m2<1, false, false>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s);
+        return am ? launch_m2<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s)
+                  : launch_m2<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s);
     }
     return am ? launch_m8<true, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s)
               : launch_m8<false, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s);
@@ -1062,12 +1160,13 @@ static cudaError_t dispatch_decode(const DecodePlan &p, float *y, const uint16_t
 
 cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                        const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
-                       int32_t *argmax, cudaStream_t s, bool pairs, const int32_t *forced)
+                       int32_t *argmax, cudaStream_t s, bool pairs, const int32_t *forced, int hblock)
 {
     const bool am = argmax != nullptr;
     const int32_t *fo = am ? forced : nullptr;
-    cudaError_t e = pairs ? dispatch_decode<true>(p, y, x, qw, sc, M, N, K, lg, keys, am, fo, s)
-                          : dispatch_decode<false>(p, y, x, qw, sc, M, N, K, lg, keys, am, fo, s);
+    const int hb = pairs ? hblock : 0;
+    cudaError_t e = pairs ? dispatch_decode<true>(p, y, x, qw, sc, M, N, K, lg, keys, am, fo, hb, s)
+                          : dispatch_decode<false>(p, y, x, qw, sc, M, N, K, lg, keys, am, fo, hb, s);
     if (e != cudaSuccess || !am)
         return e;
     return run_argmax_finalize(argmax, keys, pairs ? M / 2 : M, p.grid, s, fo);

@@ -14,7 +14,9 @@
 // decode tolerance). The parts are written as x-rows 2m and 2m+1 of a scratch
 // activation; the decode kernels run on the 2M rows and add each pair before
 // storing. For M = 1 the pair fills the mma columns that a single row leaves
-// empty, so the split costs no tensor work and no extra weight traffic.
+// empty, so the split costs no tensor work and no extra weight traffic. For
+// M = 1 with blocks of 256 or 512 the decode kernel itself performs the same
+// stages while it stages x (gemv_decode.cu), and this kernel is not launched.
 #include "common.cuh"
 #include "internal.h"
 

@@ -37,10 +37,13 @@ size_t decode_smem_bytes(const DecodePlan &p, int M, int K);
 // its pair's products (M even; M == 2 or M <= 8 by the plan's kernel).
 // forced (argmax only, M <= 2 kernels): when *forced >= 0 as the kernels start,
 // no weight is read, y is left as it was and argmax[m] = *forced.
+// hblock (pairs, M = 2, the M <= 2 kernels, K % 128 == 0, hblock 256 or 512):
+// x is ONE row and the kernel forms the (hi, lo) rows of x H itself (blocks of
+// hblock) while staging x.
 cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
                        const uint16_t *sc, int M, int N, int K, int lg, unsigned long long *keys,
                        int32_t *argmax, cudaStream_t s, bool pairs = false,
-                       const int32_t *forced = nullptr);
+                       const int32_t *forced = nullptr, int hblock = 0);
 
 // Bulk-copy streaming decode kernel (M <= 2, K % 256 == 0, 16-byte aligned
 // codes and steps): cluster size C splits K, nclusters split the row blocks.

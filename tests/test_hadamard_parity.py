@@ -32,7 +32,11 @@ def w4():
 @pytest.mark.parametrize("M,N,K,b,group", [(1, 2560, 1536, 512, 32), (1, 1536, 6144, 256, 256),
                                            (2, 300, 2048, 128, 64), (3, 500, 1024, 32, 32),
                                            (4, 2560, 1536, 512, 256), (1, 70, 512, 2, 32),
-                                           (1, 33, 4096, 4096, 512), (2, 1536, 12288, 512, 256)])
+                                           (1, 33, 4096, 4096, 512), (2, 1536, 12288, 512, 256),
+                                           # fused into the decode kernel's staging (M = 1, blocks of
+                                           # 256 / 512): many blocks per warp, one block, ragged N
+                                           (1, 1536, 12288, 512, 256), (1, 48, 256, 256, 32),
+                                           (1, 4000, 2048, 256, 64)])
 def test_rotated_gemv_matches_oracle(w4, M, N, K, b, group):
     import torch
     x = synth.gen_x(900 + M + b, M, K)
