@@ -102,7 +102,8 @@ __device__ __forceinline__ void stage_x_rows_async(uint4 *xs, const uint16_t *x,
 }
 
 // Fused rotation for the Hadamard-rotated GEMV at M = 1 (blocks of b = 32 * PL
-// values, PL = 8 or 16, K % 128 == 0): x-rows 0, 1 of xs become hi = bf16(v),
+// values, PL = 8 or 16, K % 128 == 0; the host routes only the M <= 2 kernel
+// here, the large-N form keeps the separate transform): x-rows 0, 1 of xs become hi = bf16(v),
 // lo = bf16(v - hi) of v = (x H)[k], permuted as stage_x_rows lays them out.
 // Warp w transforms blocks w, w + nwarps, ...: lane l holds values
 // [PL*l, PL*l + PL) of the block in registers, so the butterfly stages over

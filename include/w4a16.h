@@ -175,8 +175,9 @@ int hbm_read_probe(unsigned long long *sum, const void *buf, size_t bytes, void 
  * 2..4096 dividing K. M in 1..4. argmax: NULL, or int32 [M] receiving the lowest
  * index of each row's maximum (as w4a16_gemv_argmax). x H is formed in fp32 and
  * carried as two bf16 parts (relative 2^-18), so the decode tolerance holds.
- * For M = 1 with hblock 256 or 512 and K % 128 == 0 the decode kernel forms
- * x H itself while it stages x (one launch, no scratch). Otherwise a separate
+ * For M = 1 with hblock 256 or 512, K % 128 == 0 and N below the vocabulary
+ * sizes (where the large-N form takes over) the decode kernel forms x H itself
+ * while it stages x (one launch, no scratch). Otherwise a separate
  * transform launch writes the rotated rows to the library's split scratch
  * (like w4a16_gemm): such calls must not run concurrently on different streams.
  * Both forms give the same bits.
