@@ -34,16 +34,23 @@ def _rank_main(rank, world, port, out_path):
         dist.destroy_process_group()
 
 
-def test_max_over_ranks_gloo(tmp_path):
+def test_max_over_ranks_gloo():
     import torch.multiprocessing as mp
     port = _free_port()
-    out = str(tmp_path / "r")
+    out_dir = os.path.join(ROOT, "_build")  # git-ignored build folder of the repo
+    os.makedirs(out_dir, exist_ok=True)
+    out = os.path.join(out_dir, f"ranks_{os.getpid()}")
     mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
-    for r in range(2):
-        with open(f"{out}.{r}") as f:
-            d = json.load(f)
-        assert d["t"] == 2.0  # the slower rank's 2 ms, seen by both
-        assert abs(d["v"] - 2 * 1_000_000 / 2e-3 / 1e9) < 1e-12
+    try:
+        for r in range(2):
+            with open(f"{out}.{r}") as f:
+                d = json.load(f)
+            assert d["t"] == 2.0  # the slower rank's 2 ms, seen by both
+            assert abs(d["v"] - 2 * 1_000_000 / 2e-3 / 1e9) < 1e-12
+    finally:
+        for r in range(2):
+            if os.path.exists(f"{out}.{r}"):
+                os.remove(f"{out}.{r}")
 
 
 def test_reference_arm_two_ranks_prints_once():
