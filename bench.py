@@ -746,6 +746,29 @@ def run_ncu_case(case: str):
         x = torch.from_numpy(synth.gen_x(1000, 1, K).view(np.int16)).to(dev)
         for _ in range(2):
             w4.w4a16_gemv_hadamard(x, q, sc, 512, group=256, argmax=True)
+    elif case == "step":
+        # One device-resident decode step of a sliding layer, twice: append into
+        # the 512-slot ring x 256 at the device position, attention at it, the
+        # group-256 LM head (262144 x 1536) with the forced-token form (not
+        # forced, then forced), the prologue.
+        H, T, D, N, K = 8, 512, 256, 262144, 1536
+        q = torch.from_numpy(synth.gen_attn_q(405, H, D).view(np.int16)).to(dev)
+        kh, vh = synth.gen_attn_kv(405, T, D)
+        k = torch.from_numpy(kh.view(np.int16)).to(dev)
+        v = torch.from_numpy(vh.view(np.int16)).to(dev)
+        kp = torch.from_numpy(synth.ring_positions(70000, T)).to(dev)
+        pos = torch.full((1,), 70001, dtype=torch.int32, device=dev)
+        lq = synth.gen_qweight_torch(1000, N, K, dev)
+        ls = torch.from_numpy(synth.gen_scales(1000, N, K, 256).view(np.int16)).to(dev)
+        x = torch.from_numpy(synth.gen_x(1000, 1, K).view(np.int16)).to(dev)
+        forced = torch.full((1,), -1, dtype=torch.int32, device=dev)
+        for rep in range(2):
+            forced.fill_(-1 if rep == 0 else 7)
+            w4.w4_kv_append(k, v, k[0].clone(), v[0].clone(), pos, kpos=kp)
+            w4.w4_attn_decode(q, k, v, kp, qpos=pos, window=T, scale=D ** -0.5)
+            _, tok = w4.w4a16_gemv_argmax_forced(x, lq, ls, forced, group=256)
+            w4.w4_decode_prologue(tok, pos, lq, ls, group=256)
+            torch.cuda.synchronize()
     elif case == "attn":
         H, T, D = 8, 131072, 512
         q = torch.from_numpy(synth.gen_attn_q(404, H, D).view(np.int16)).to(dev)
