@@ -118,3 +118,23 @@ def test_read_probe_closed_form(w4):
     s = w4.hbm_read_probe(buf)
     torch.cuda.synchronize()
     assert int(s.item()) == n * (n - 1) // 2
+
+
+def test_gather_word_aligned_table_takes_the_word_path(w4):
+    """A table only 4-byte aligned (allowed by the header) is gathered one word
+    per thread; a 16-byte-aligned one a group per thread. Both bit-exact."""
+    import torch
+    N, K = 300, 2048
+    qt = synth.gen_qweight(870, N, K)
+    sc = synth.gen_scales(870, N, K)
+    ids = synth.gen_ids(871, 64, N)
+    ref, _ = oracle.embed_gather(ids, qt, sc)
+    flat = torch.empty(N * (K // 8) + 1, dtype=torch.int32, device="cuda")
+    flat[1:] = torch.from_numpy(qt.view(np.int32).ravel()).cuda()
+    q_word = flat[1:].view(N, K // 8)
+    assert q_word.data_ptr() % 16 != 0
+    ids_d = torch.from_numpy(ids.astype(np.int32)).cuda()
+    for q in (q_word, to_dev_u32(qt)):
+        out = w4.w4_embed_gather(ids_d, q, to_dev_bits16(sc))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits16(out), ref)
