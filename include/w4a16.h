@@ -282,7 +282,8 @@ int w4a16_gemv_argmax_forced(float *y, int32_t *argmax, const uint16_t *x, const
  * 64, 128, 256 or 512); x_next bf16 [K] (16-byte aligned); pos, token, tokens,
  * status int32 (4-byte aligned). A token outside [0, V) gives a zero row and
  * sets bit 0 of *status; a full history sets bit 1 (status may be NULL; bits
- * are only ever set). The position is read and written when the kernel runs.
+ * are only ever set). The position is read and written when the kernel runs;
+ * it must stay below 2^31 - 1 (the increment is not checked for overflow).
  */
 int w4_decode_prologue(uint16_t *x_next, int32_t *tokens, int32_t *pos, const int32_t *token,
                        const uint32_t *qtable, const uint16_t *scales, int V, int K, int group, int cap,
