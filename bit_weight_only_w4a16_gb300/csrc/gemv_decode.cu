@@ -874,6 +874,167 @@ gemv_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                             reinterpret_cast<float *>(xs + 8 * cpr), keys);
 }
 
+// Large N at M <= 8 (the vocabulary projection for up to 8 x-rows): the quad
+// kernel's loads and compute, with each warp walking row blocks gw, gw + GW, ...
+// of the whole grid as one stream of k-quads (U in flight, the pipeline never
+// drains between row blocks), as the M <= 2 large-N form does. A row block's
+// outputs (and argmax keys) are stored when its last quad is computed.
+// K % 128 == 0, N % 16 == 0, 8-byte-aligned steps; two CTAs of 8 warps per SM.
+template <int U, bool ARGMAX, bool PAIRS>
+__global__ void __launch_bounds__(256, 2)
+gemv_m8q_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+                        const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc, int M, int N, int K,
+                        unsigned long long *__restrict__ keys, int lg, int sc8)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int nrb = N >> 4;
+    const int ngroups = K >> 5, nq = ngroups >> 2;
+    const int GW = gridDim.x * 8, gw = blockIdx.x * 8 + warp;
+    const int nmine = nrb > gw ? (nrb - gw + GW - 1) / GW : 0;
+    const int Qt = nmine * nq; // k-quads of this warp, row block by row block
+    const int sstride = ngroups >> lg;
+
+    // Loader cursor: row A of the warp's current row block (row B is 8 rows on)
+    // and the quad within it.
+    const uint32_t *lpA = qw + (size_t)(gw * 16 + g) * (K >> 3) + 4 * t;
+    const uint16_t *lsA = sc + (size_t)(gw * 16 + g) * sstride;
+    const size_t rowB_words = (size_t)8 * (K >> 3), rowB_steps = (size_t)8 * sstride;
+    const size_t rb_words = (size_t)GW * 16 * (K >> 3), rb_steps = (size_t)GW * 16 * sstride;
+    int lq = 0;
+
+    uint4 wa[U], wb[U];
+    uint2 sa[U], sb[U];
+    auto steps4 = [&](const uint16_t *srow, int Q) -> uint2 {
+        if (!sc8) { // steps not 8-byte aligned: four 16-bit loads
+            uint32_t v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                v[j] = ldg_nc_u16(srow + ((4 * Q + j) >> lg));
+            return make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+        }
+        if (lg == 0)
+            return ldg_nc_u64(srow + 4 * Q);
+        if (lg == 1) {
+            const uint32_t v = ldg_nc_u32(srow + 2 * Q);
+            return make_uint2((v & 0xFFFFu) | (v << 16), (v >> 16) | (v & 0xFFFF0000u));
+        }
+        const uint32_t v = ldg_nc_u16(srow + ((4 * Q) >> lg));
+        return make_uint2(v | (v << 16), v | (v << 16));
+    };
+    auto load = [&](int u) {
+        wa[u] = ldg_stream_v4(lpA + 16 * lq);
+        wb[u] = ldg_stream_v4(lpA + rowB_words + 16 * lq);
+        sa[u] = steps4(lsA, lq);
+        sb[u] = steps4(lsA + rowB_steps, lq);
+        if (++lq == nq) {
+            lq = 0;
+            lpA += rb_words;
+            lsA += rb_steps;
+        }
+    };
+
+    if (threadIdx.x == 32)
+        prefetch_l2_bulk(x, (uint32_t)(M * K * 2));
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (u < Qt)
+            load(u);
+    pdl_launch_dependents();
+    pdl_wait();
+
+    uint4 *xs = reinterpret_cast<uint4 *>(smem); // [8][K/8] permuted chunks
+    const int cpr = K >> 3;
+    stage_x_rows_async(xs, x, M, K);
+    if (M < 8) // rows M..7 of the B operand are zero
+        for (int i = M * cpr + threadIdx.x; i < 8 * cpr; i += blockDim.x)
+            xs[i] = make_uint4(0u, 0u, 0u, 0u);
+    __shared__ unsigned long long ck[8];
+    if (ARGMAX && threadIdx.x < 8)
+        ck[threadIdx.x] = 0ull;
+    __syncthreads();
+
+    // B column g is x-row g; this lane supplies word t of each group.
+    const uint4 *xrow = xs + g * cpr + t;
+    const int Mout = PAIRS ? M / 2 : M;
+    const int m0 = PAIRS ? t : 2 * t, m1 = 2 * t + 1;
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+    int cq = 0, crb = 0; // compute cursor: quad and row block (j-th of this warp)
+
+    auto finish = [&]() {
+        // Row block gw + crb * GW: lane (g, t) holds y[2t][rowA], y[2t+1][rowA],
+        // y[2t][rowB], y[2t+1][rowB] (N % 16 == 0: both rows exist).
+        if (PAIRS) {
+            a0 += a1;
+            b0 += b1;
+        }
+        const int rowA = (gw + crb * GW) * 16 + g, rowB = rowA + 8;
+        const float v[2][2] = {{a0, a1}, {b0, b1}};
+        const int rows[2] = {rowA, rowB};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int j = 0; j < (PAIRS ? 1 : 2); ++j) {
+                const int mm = j ? m1 : m0;
+                if (mm < Mout) {
+                    y[(size_t)mm * N + rows[h]] = v[h][j];
+                    if (ARGMAX)
+                        atomicMax(&ck[mm], argmax_key(v[h][j], rows[h]));
+                }
+            }
+        }
+        a0 = a1 = b0 = b1 = 0.f;
+    };
+
+    auto compute = [&](int u) {
+        uint32_t va[4] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w};
+        uint32_t vb[4] = {wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+        quad_transpose4(va, t);
+        quad_transpose4(vb, t);
+        const uint32_t sw_a[2] = {sa[u].x, sa[u].y}, sw_b[2] = {sb[u].x, sb[u].y};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int G = 4 * cq + j;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint4 bx = xrow[4 * G];
+            uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+            unpack_word(va[j], a04, a15, a26, a37);
+            unpack_word(vb[j], b04, b15, b26, b37);
+            mma_16816(c, a04, b04, a15, b15, bx.x, bx.y);
+            mma_16816(c, a26, b26, a37, b37, bx.z, bx.w);
+            const float s_a = (j & 1) ? bf16hi_to_f32(sw_a[j >> 1]) : bf16lo_to_f32(sw_a[j >> 1]);
+            const float s_b = (j & 1) ? bf16hi_to_f32(sw_b[j >> 1]) : bf16lo_to_f32(sw_b[j >> 1]);
+            a0 = fmaf(s_a, c[0], a0);
+            a1 = fmaf(s_a, c[1], a1);
+            b0 = fmaf(s_b, c[2], b0);
+            b1 = fmaf(s_b, c[3], b1);
+        }
+        if (++cq == nq) {
+            finish();
+            cq = 0;
+            ++crb;
+        }
+    };
+
+    for (int base = 0; base < Qt; base += U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (base + u < Qt) {
+                compute(u);
+                if (base + u + U < Qt)
+                    load(u);
+            }
+        }
+    }
+
+    if (ARGMAX) {
+        __syncthreads();
+        if (threadIdx.x < Mout)
+            keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
+    }
+}
+
 // ---------------------------------------------------- argmax finalize ----
 
 __global__ void __launch_bounds__(256)
@@ -1018,6 +1179,16 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
             const int per_sm = (65536 / (96 * 32)) / q.warps;
             return (long long)q.grid <= (long long)num_sms * per_sm;
         };
+        if (K % kTileK == 0 && N % 16 == 0 && nrb >= 2 * num_sms * 16) {
+            // Vocabulary-sized N: the persistent form, two CTAs of 8 warps per
+            // SM, each warp walking at least two row blocks per wave.
+            p.kernel = 9;
+            p.ksplit = 1;
+            p.warps = 8;
+            p.unroll = 4;
+            p.grid = 2 * num_sms;
+            return p;
+        }
         if (nrb >= 2 * num_sms && K % kTileK == 0) {
             // Many row blocks: as for M <= 2, one CTA per SM holding
             // ceil(nrb / SMs) row blocks, K split as far as 16 warps allow;
@@ -1110,11 +1281,27 @@ static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, c
                       p.ksplit, keys, lg);
 }
 
+template <bool ARGMAX, bool PAIRS>
+static cudaError_t launch_m8p(const DecodePlan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                              const uint16_t *sc, int M, int N, int K, unsigned long long *keys, int lg,
+                              cudaStream_t s)
+{
+    const size_t smem = (size_t)8 * K * 2;
+    auto kern = gemv_m8q_persist_kernel<4, ARGMAX, PAIRS>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    const int sc8 = (reinterpret_cast<uintptr_t>(sc) & 7) == 0 ? 1 : 0;
+    return launch_pdl(kern, dim3(p.grid), dim3(256), smem, s, y, x, qw, sc, M, N, K, keys, lg, sc8);
+}
+
 size_t decode_smem_bytes(const DecodePlan &p, int M, int K)
 {
     const size_t rbc = (size_t)(p.warps / p.ksplit);
     if (p.kernel == 3)
         return (size_t)M * K * 2 + 16;
+    if (p.kernel == 9)
+        return (size_t)8 * K * 2;
     if (p.kernel == 2)
         return (size_t)M * ((K + kTileK - 1) / kTileK * kTileK) * 2 + 16 +
                (p.ksplit > 1 ? rbc * p.ksplit * M * 16 * sizeof(float) : 0);
@@ -1155,6 +1342,9 @@ static cudaError_t dispatch_decode(const DecodePlan &p, float *y, const uint16_t
         return am ? launch_m2<2, true, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s)
                   : launch_m2<2, false, PAIRS>(p, y, x, qw, sc, N, K, keys, lg, fo, hb, s);
     }
+    if (p.kernel == 9)
+        return am ? launch_m8p<true, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s)
+                  : launch_m8p<false, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s);
     return am ? launch_m8<true, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s)
               : launch_m8<false, PAIRS>(p, y, x, qw, sc, M, N, K, keys, lg, s);
 }

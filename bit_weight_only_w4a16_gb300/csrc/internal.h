@@ -19,7 +19,7 @@ inline int group_shift(int group)
 // Per-shape launch plan of the decode kernels (M <= 8).
 struct DecodePlan {
     int kernel = 2; // 2: M <= 2 kernel (full-group 128-bit loads), 3: its persistent form for
-                    // very large N, 8: M <= 8 kernel
+                    // very large N, 8: M <= 8 kernel, 9: its persistent form for very large N
     int ksplit = 1; // warps of a CTA that split K for one 16-row block
     int warps = 8;  // warps per CTA
     int unroll = 4; // k-tiles (m2) or groups (m8) in flight per warp

@@ -52,6 +52,10 @@ def _addr(v):
 
 
 def test_validation_before_any_launch(lib):
+    import torch
+    if torch.cuda.is_available():
+        # Fake addresses: never handed to a machine where a launch could use them.
+        pytest.skip("host-only check (a GPU is present)")
     l, _ = lib
     A = _addr(1 << 20)  # a 16-byte aligned non-NULL address; never dereferenced
     # NULL pointer

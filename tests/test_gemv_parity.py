@@ -195,10 +195,11 @@ def test_vocab_projection_with_argmax(w4):
     assert int(a[0]) == int(np.argmax(y[0]))
 
 
-@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
 def test_large_n_sampled_rows_and_argmax(w4, M):
-    # N = 80000 (5000 row blocks: the persistent large-N form on a 152-SM GPU),
-    # K = 1536; logits on sampled rows plus the exact greedy pick per x-row.
+    # N = 80000 (5000 row blocks: the persistent large-N forms on a 152-SM GPU,
+    # M <= 2 and M <= 8), K = 1536; logits on sampled rows plus the exact greedy
+    # pick per x-row.
     import torch
     N, K, seed = 80000, 1536, 1100 + M
     x = synth.gen_x(seed, M, K)
@@ -243,3 +244,26 @@ def test_streaming_and_register_kernels_agree_with_oracle(w4, M):
 
 def test_no_device_error_reported(w4):
     assert w4.device_error() == 0
+
+
+def test_large_n_m8_steps_only_4_byte_aligned(w4):
+    """The M <= 8 large-N form with a step table 4-byte but not 8-byte aligned
+    (allowed by the header): the step loads fall back to 16-bit ones; same bits
+    as the 8-byte-aligned call."""
+    import torch
+    M, N, K, seed = 8, 80000, 1536, 1190
+    x = synth.gen_x(seed, M, K)
+    qd = synth.gen_qweight_torch(seed, N, K, "cuda")
+    sc = synth.gen_scales(seed, N, K)
+    flat = torch.empty(N * (K // 32) + 2, dtype=torch.int16, device="cuda")
+    flat[2:] = torch.from_numpy(sc.view(np.int16).ravel()).cuda()
+    sc4 = flat[2:].view(N, K // 32)
+    assert sc4.data_ptr() % 8 == 4
+    xd = to_dev_bits16(x)
+    y4, a4 = w4.w4a16_gemv_argmax(xd, qd, sc4)
+    y8, a8 = w4.w4a16_gemv_argmax(xd, qd, to_dev_bits16(sc))
+    torch.cuda.synchronize()
+    assert torch.equal(y4, y8) and torch.equal(a4, a8)
+    rows = np.array([0, 1, 40000, N - 1])
+    yr, ar = oracle.gemm(x, synth.gen_qweight_rows(seed, N, K, rows), sc[rows])
+    assert_w4_close(y4.cpu().numpy()[:, rows], yr, ar, what="large N M8, 4-byte-aligned steps")

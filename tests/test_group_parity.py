@@ -63,7 +63,7 @@ def test_decode_group64_k_not_tile_multiple(w4, M):
     assert_w4_close(y.cpu().numpy(), yr, ar, what=f"decode g64 K320 M{M}")
 
 
-@pytest.mark.parametrize("M", [1, 2])
+@pytest.mark.parametrize("M", [1, 2, 8])
 def test_large_n_group256_argmax(w4, M):
     """The vocabulary-projection form (persistent kernel) with the LM head's group 256."""
     import torch

@@ -48,22 +48,25 @@ def test_rotated_gemv_matches_oracle(w4, M, N, K, b, group):
     assert_w4_close(y.cpu().numpy(), yr, ar, what=f"hadamard M{M} N{N} K{K} b{b} g{group}")
 
 
-def test_rotated_lm_head_argmax(w4):
-    """The vocabulary-projection form (persistent kernel) with the LM head's group
-    256 and the fused greedy pick."""
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_rotated_lm_head_argmax(w4, M):
+    """The vocabulary-projection forms (persistent kernels; at M = 2..4 the pair
+    rows take the M <= 8 one) with the LM head's group 256 and the fused greedy
+    pick."""
     import torch
-    M, N, K, b, group = 1, 80000, 1536, 512, 256
-    x = synth.gen_x(950, M, K)
+    N, K, b, group = 80000, 1536, 512, 256
+    x = synth.gen_x(950 + M, M, K)
     qw = synth.gen_qweight(951, N, K)
     sc = synth.gen_scales(951, N, K, group)
     q = synth.gen_qweight_torch(951, N, K, torch.device("cuda"))
     y, a = w4.w4a16_gemv_hadamard(to_dev_bits16(x), q, to_dev_bits16(sc), b, group=group, argmax=True)
     torch.cuda.synchronize()
     yr, ar = oracle.gemm_hadamard(x, qw, sc, b, group)
-    assert_w4_close(y.cpu().numpy(), yr, ar, what="rotated LM head")
-    idx, gap = oracle.argmax(yr[0])
-    assert gap > 2 * (1e-4 * ar[0, idx] + 1e-6), "ambiguous seed"
-    assert int(a.cpu().numpy()[0]) == idx
+    assert_w4_close(y.cpu().numpy(), yr, ar, what=f"rotated LM head M{M}")
+    for m in range(M):
+        idx, gap = oracle.argmax(yr[m])
+        assert gap > 2 * (1e-4 * ar[m, idx] + 1e-6), "ambiguous seed"
+        assert int(a.cpu().numpy()[m]) == idx
 
 
 def test_fused_rotation_matches_a_prerotated_activation(w4):

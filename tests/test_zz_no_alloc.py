@@ -45,7 +45,20 @@ def test_noalloc_matches_regular_on_two_calls(w4, M, N, K):
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(w4):
-    # Checked on the host before any launch: the pointers are never touched.
-    A = ctypes.c_void_p(1 << 20)
-    rc = w4._lib.w4a16_gemv_argmax_noalloc(A, A, A, A, A, 8, 1 << 22, 256, 32, None)
+    """A call whose plan needs more argmax keys than the fixed scratch holds is
+    refused on the host. K = 160 (not a multiple of 128) keeps the large-N forms
+    out, so 8 x-rows over 2^22 rows need 8 x 32768 keys against 32768. The
+    buffers are real (zeroed), so no plan could make the call touch an invalid
+    address."""
+    import torch
+    M, N, K = 8, 1 << 22, 160
+    y = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    a = torch.zeros((M,), dtype=torch.int32, device="cuda")
+    x = torch.zeros((M, K), dtype=torch.int16, device="cuda")
+    q = torch.zeros((N, K // 8), dtype=torch.int32, device="cuda")
+    sc = torch.zeros((N, K // 32), dtype=torch.int16, device="cuda")
+    P = ctypes.c_void_p
+    rc = w4._lib.w4a16_gemv_argmax_noalloc(P(y.data_ptr()), P(a.data_ptr()), P(x.data_ptr()), P(q.data_ptr()),
+                                           P(sc.data_ptr()), M, N, K, 32, None)
+    torch.cuda.synchronize()
     assert rc == 2
