@@ -27,22 +27,6 @@ struct DeviceState {
 
 DeviceState g_dev[kMaxDevices];
 
-// Decode kernel selection: W4_DECODE_PATH=stream | register forces one of the
-// two decode kernels (both compute the full result; used by the tests and the
-// per-shape tuning sweep). Unset or anything else: the per-shape table.
-enum DecodePath { kPathAuto = 0, kPathStream = 1, kPathRegister = 2 };
-DecodePath decode_path()
-{
-    static const DecodePath p = [] {
-        const char *e = std::getenv("W4_DECODE_PATH");
-        if (e && std::strcmp(e, "stream") == 0)
-            return kPathStream;
-        if (e && std::strcmp(e, "register") == 0)
-            return kPathRegister;
-        return kPathAuto;
-    }();
-    return p;
-}
 std::mutex g_mu;
 thread_local char g_cuda_err[256] = "";
 
@@ -146,19 +130,6 @@ bool decode_fits(const w4::DecodePlan &p, int M, int K)
     return w4::decode_smem_bytes(p, M, K) <= 220 * 1024;
 }
 
-// Which decode kernel serves (M, N, K): the tensor-copy streaming kernel where
-// it measured faster on GB300, the register-streaming kernel otherwise.
-bool use_stream(int M, int N, int K, const void *qw, const void *sc)
-{
-    if (!w4::stream_supported(M, N, K, qw, sc))
-        return false;
-    switch (decode_path()) {
-    case kPathStream: return true;
-    case kPathRegister: return false;
-    default: return w4::stream_preferred(M, N, K);
-    }
-}
-
 } // namespace
 
 extern "C" {
@@ -197,11 +168,10 @@ int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int lg = w4::group_shift(group);
-    if (lg == 0 && use_stream(M, N, K, qweight, scales)) {
-        const w4::StreamPlan sp = w4::plan_stream(M, N, K, st->num_sms);
-        if (sp.ok) {
-            cudaError_t e = w4::run_stream(sp, y, x, qweight, scales, M, N, K, nullptr, nullptr,
-                                           st->err, s);
+    if (M == 1) {
+        const w4::M1Plan mp = w4::plan_decode_m1(M, N, K, st->num_sms);
+        if (mp.ok) {
+            cudaError_t e = w4::run_decode_m1(mp, y, x, qweight, scales, N, K, lg, s);
             return e == cudaSuccess ? W4_OK : cuda_fail(e);
         }
     }
@@ -250,14 +220,6 @@ int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int lg = w4::group_shift(group);
-    if (lg == 0 && use_stream(M, N, K, qweight, scales)) {
-        const w4::StreamPlan sp = w4::plan_stream(M, N, K, st->num_sms);
-        if (sp.ok && (size_t)M * sp.C * sp.nclusters <= kKeyCapacity) {
-            cudaError_t e = w4::run_stream(sp, y, x, qweight, scales, M, N, K, st->keys, argmax,
-                                           st->err, s);
-            return e == cudaSuccess ? W4_OK : cuda_fail(e);
-        }
-    }
     const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
     if (!decode_fits(p, M, K) || (size_t)M * p.grid > kKeyCapacity)
         return W4_ERR_UNSUPPORTED;

@@ -189,7 +189,7 @@ __device__ __forceinline__ void stage_x_hadamard(uint4 *xs, const uint16_t *x, i
 // parts of an fp32 value); each output row is the sum of its pair.
 template <int MX, int U, bool SC32, bool FULL, bool ARGMAX, bool G32, bool PAIRS>
 __global__ void __launch_bounds__(512)
-gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+w4_decode_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
                int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg,
                const int32_t *__restrict__ forced, int hb, float hnorm)
@@ -408,7 +408,7 @@ gemv_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 // then beat 6, 8 or 12 (46.3 vs 48.1, 49.0, 63.0 us) and 3 or 4 CTAs per SM.
 template <int MX, int U, int MINB, bool ARGMAX, bool G32, bool PAIRS>
 __global__ void __launch_bounds__(256, MINB)
-gemv_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+w4_decode_m2_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                        const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc, int N, int K,
                        unsigned long long *__restrict__ keys, int lg, const int32_t *__restrict__ forced,
                        int hb, float hnorm)
@@ -673,7 +673,7 @@ __device__ __forceinline__ void m8_store(float *__restrict__ y, float a0, float 
 
 template <int U, bool ARGMAX, bool PAIRS>
 __global__ void __launch_bounds__(512)
-gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+w4_decode_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
                int M, int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg)
 {
@@ -764,7 +764,7 @@ gemv_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 // U = 8 (8 quads in flight, ~160 registers) runs CTAs of at most 12 warps.
 template <int U, bool ARGMAX, bool PAIRS>
 __global__ void __launch_bounds__(U == 8 ? 384 : 512)
-gemv_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+w4_decode_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
                int M, int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg)
 {
@@ -882,7 +882,7 @@ gemv_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 // K % 128 == 0, N % 16 == 0, 8-byte-aligned steps; two CTAs of 8 warps per SM.
 template <int U, bool ARGMAX, bool PAIRS>
 __global__ void __launch_bounds__(256, 2)
-gemv_m8q_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
+w4_decode_m8q_persist_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                         const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc, int M, int N, int K,
                         unsigned long long *__restrict__ keys, int lg, int sc8)
 {
@@ -1238,20 +1238,20 @@ static cudaError_t launch_m2(const DecodePlan &p, float *y, const uint16_t *x, c
 
     const bool sc32 = (K % 64) == 0, full = (K % kTileK) == 0;
     // Groups above 32 take the same kernels with a run-time step shift.
-    auto kern = sc32 ? gemv_m2_kernel<MX, 4, true, false, ARGMAX, true, PAIRS>
-                     : gemv_m2_kernel<MX, 4, false, false, ARGMAX, true, PAIRS>;
+    auto kern = sc32 ? w4_decode_m2_kernel<MX, 4, true, false, ARGMAX, true, PAIRS>
+                     : w4_decode_m2_kernel<MX, 4, false, false, ARGMAX, true, PAIRS>;
     if (p.unroll == 8)
-        kern = sc32 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX, true, PAIRS>
-                    : gemv_m2_kernel<MX, 8, false, false, ARGMAX, true, PAIRS>;
+        kern = sc32 ? w4_decode_m2_kernel<MX, 8, true, false, ARGMAX, true, PAIRS>
+                    : w4_decode_m2_kernel<MX, 8, false, false, ARGMAX, true, PAIRS>;
     if (full)
-        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX, true, PAIRS>
-                             : gemv_m2_kernel<MX, 4, true, true, ARGMAX, true, PAIRS>;
+        kern = p.unroll == 8 ? w4_decode_m2_kernel<MX, 8, true, true, ARGMAX, true, PAIRS>
+                             : w4_decode_m2_kernel<MX, 4, true, true, ARGMAX, true, PAIRS>;
     if (lg > 0) { // K % 64 == 0 here
-        kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, false, ARGMAX, false, PAIRS>
-                             : gemv_m2_kernel<MX, 4, true, false, ARGMAX, false, PAIRS>;
+        kern = p.unroll == 8 ? w4_decode_m2_kernel<MX, 8, true, false, ARGMAX, false, PAIRS>
+                             : w4_decode_m2_kernel<MX, 4, true, false, ARGMAX, false, PAIRS>;
         if (full)
-            kern = p.unroll == 8 ? gemv_m2_kernel<MX, 8, true, true, ARGMAX, false, PAIRS>
-                                 : gemv_m2_kernel<MX, 4, true, true, ARGMAX, false, PAIRS>;
+            kern = p.unroll == 8 ? w4_decode_m2_kernel<MX, 8, true, true, ARGMAX, false, PAIRS>
+                                 : w4_decode_m2_kernel<MX, 4, true, true, ARGMAX, false, PAIRS>;
     }
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
@@ -1269,11 +1269,11 @@ static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, c
     size_t smem = (size_t)8 * K * 2;
     if (p.ksplit > 1)
         smem += (size_t)rbc * p.ksplit * 8 * 16 * sizeof(float);
-    auto kern = gemv_m8_kernel<8, ARGMAX, PAIRS>;
+    auto kern = w4_decode_m8_kernel<8, ARGMAX, PAIRS>;
     // 128-bit code loads with a quad transpose when K % 128 == 0 and the steps
     // allow 8-byte loads.
     if (K % kTileK == 0 && (reinterpret_cast<uintptr_t>(sc) & 7) == 0)
-        kern = p.unroll == 8 ? gemv_m8q_kernel<8, ARGMAX, PAIRS> : gemv_m8q_kernel<4, ARGMAX, PAIRS>;
+        kern = p.unroll == 8 ? w4_decode_m8q_kernel<8, ARGMAX, PAIRS> : w4_decode_m8q_kernel<4, ARGMAX, PAIRS>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
@@ -1287,7 +1287,7 @@ static cudaError_t launch_m8p(const DecodePlan &p, float *y, const uint16_t *x, 
                               cudaStream_t s)
 {
     const size_t smem = (size_t)8 * K * 2;
-    auto kern = gemv_m8q_persist_kernel<4, ARGMAX, PAIRS>;
+    auto kern = w4_decode_m8q_persist_kernel<4, ARGMAX, PAIRS>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
@@ -1314,8 +1314,8 @@ static cudaError_t launch_persist(const DecodePlan &p, float *y, const uint16_t 
                                   const int32_t *forced, int hb, cudaStream_t s)
 {
     const size_t smem = (size_t)MX * K * 2 + 16;
-    auto kern = lg == 0 ? gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, true, PAIRS>
-                        : gemv_m2_persist_kernel<MX, 4, 2, ARGMAX, false, PAIRS>;
+    auto kern = lg == 0 ? w4_decode_m2_persist_kernel<MX, 4, 2, ARGMAX, true, PAIRS>
+                        : w4_decode_m2_persist_kernel<MX, 4, 2, ARGMAX, false, PAIRS>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;

@@ -45,22 +45,17 @@ cudaError_t run_decode(const DecodePlan &p, float *y, const uint16_t *x, const u
                        int32_t *argmax, cudaStream_t s, bool pairs = false,
                        const int32_t *forced = nullptr, int hblock = 0);
 
-// Bulk-copy streaming decode kernel (M <= 2, K % 256 == 0, 16-byte aligned
-// codes and steps): cluster size C splits K, nclusters split the row blocks.
-struct StreamPlan {
-    int C = 1;
-    int nclusters = 1;
-    int sr = 1; // 16-row blocks per stage
+// M = 1 decode GEMV (K % 128 == 0, N % 16 == 0, below vocabulary sizes): a CTA
+// of `warps` warps owns R 16-row blocks; K (T tiles of 128) is split into S
+// sub-slices, one per warp of a row block.
+struct M1Plan {
     bool ok = false;
+    int R = 1, S = 1, T = 1, warps = 8, grid = 1;
 };
 
-bool stream_supported(int M, int N, int K, const void *qw, const void *sc);
-// Per-shape choice between the two decode kernels (from measurements on GB300).
-bool stream_preferred(int M, int N, int K);
-StreamPlan plan_stream(int M, int N, int K, int num_sms);
-cudaError_t run_stream(const StreamPlan &p, float *y, const uint16_t *x, const uint32_t *qw,
-                       const uint16_t *sc, int M, int N, int K, unsigned long long *keys,
-                       int32_t *argmax, int *err, cudaStream_t s);
+M1Plan plan_decode_m1(int M, int N, int K, int num_sms);
+cudaError_t run_decode_m1(const M1Plan &p, float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc,
+                          int N, int K, int lg, cudaStream_t s);
 
 // argmax[m] = index of the largest key in keys[m][0 .. nblocks), or *forced
 // when forced != nullptr and *forced >= 0.
