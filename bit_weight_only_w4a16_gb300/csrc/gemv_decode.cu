@@ -323,13 +323,57 @@ w4_decode_m2_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         }
     };
 
-    for (int base = 0; base < nkt; base += U) {
+    // Two tiles at once (four independent mma chains, twice the independent
+    // unpack work between dependent instructions); the same sums in the same
+    // order as one tile at a time.
+    auto compute2 = [&](int u, int kt) {
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, d0[4] = {0.f, 0.f, 0.f, 0.f};
+        float c1[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4 *xb = xrow + xstep * kt;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (base + u < nkt) {
-                compute(u, kt0 + base + u);
-                if (base + u + U < nkt)
-                    load(u, kt0 + base + u + U);
+        for (int i = 0; i < 4; ++i) {
+            const uint4 b0 = xb[xi * i], b1 = xb[xstep + xi * i];
+            unpack_mma2(c0, d0, (&wa[u].x)[i], (&wb[u].x)[i], b0.x, b0.y, b0.z, b0.w);
+            unpack_mma2(c1, d1, (&wa[u + 1].x)[i], (&wb[u + 1].x)[i], b1.x, b1.y, b1.z, b1.w);
+        }
+        if (G32) {
+            accA = fmaf(bf16lo_to_f32(sa[u]), c0[0] + d0[0], accA);
+            accA = fmaf(bf16hi_to_f32(sa[u]), c0[1] + d0[1], accA);
+            accB = fmaf(bf16lo_to_f32(sb[u]), c0[2] + d0[2], accB);
+            accB = fmaf(bf16hi_to_f32(sb[u]), c0[3] + d0[3], accB);
+            accA = fmaf(bf16lo_to_f32(sa[u + 1]), c1[0] + d1[0], accA);
+            accA = fmaf(bf16hi_to_f32(sa[u + 1]), c1[1] + d1[1], accA);
+            accB = fmaf(bf16lo_to_f32(sb[u + 1]), c1[2] + d1[2], accB);
+            accB = fmaf(bf16hi_to_f32(sb[u + 1]), c1[3] + d1[3], accB);
+        } else {
+            accA = fmaf(bf16lo_to_f32(sa[u]), (c0[0] + d0[0]) + (c0[1] + d0[1]), accA);
+            accB = fmaf(bf16lo_to_f32(sb[u]), (c0[2] + d0[2]) + (c0[3] + d0[3]), accB);
+            accA = fmaf(bf16lo_to_f32(sa[u + 1]), (c1[0] + d1[0]) + (c1[1] + d1[1]), accA);
+            accB = fmaf(bf16lo_to_f32(sb[u + 1]), (c1[2] + d1[2]) + (c1[3] + d1[3]), accB);
+        }
+    };
+
+    // Measured on GB300 in the graph-replayed decode sweep: pairs pay where a
+    // warp's tiles are all preloaded (1536 x 12288: 5.50 -> 5.39 us) and lose
+    // where tiles are refilled, since a pair delays its two refills
+    // (24576 x 1536: 6.95 -> 7.82 us).
+    if (U == 8 && MX == 1 && nkt <= U) {
+#pragma unroll
+        for (int u = 0; u < U; u += 2) {
+            if (u + 1 < nkt)
+                compute2(u, kt0 + u);
+            else if (u < nkt)
+                compute(u, kt0 + u);
+        }
+    } else {
+        for (int base = 0; base < nkt; base += U) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (base + u < nkt) {
+                    compute(u, kt0 + base + u);
+                    if (base + u + U < nkt)
+                        load(u, kt0 + base + u + U);
+                }
             }
         }
     }
