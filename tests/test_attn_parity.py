@@ -16,13 +16,14 @@ import oracle
 import synth
 
 from _util import to_dev_bits16
+from _guard import guarded
 
 pytestmark = pytest.mark.gpu
 
 
 def _w4():
     import bit_weight_only_w4a16_gb300 as w4
-    return w4
+    return guarded(w4)
 
 
 def _score_scale(q, k, keep, scale):

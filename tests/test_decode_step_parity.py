@@ -22,6 +22,7 @@ import pytest
 import oracle
 import synth
 from _util import assert_w4_close, bits16, to_dev_bits16, to_dev_u32
+from _guard import check_all, gempty, gfrom, gfull, guarded, gzeros
 
 pytestmark = pytest.mark.gpu
 
@@ -33,12 +34,11 @@ def w4():
         pytest.skip("no GPU")
     import bit_weight_only_w4a16_gb300 as w4
     w4.init()
-    return w4
+    return guarded(w4)
 
 
 def _i32(v):
-    import torch
-    return torch.tensor(np.atleast_1d(np.asarray(v, dtype=np.int32)), device="cuda")
+    return gfrom(np.atleast_1d(np.asarray(v, dtype=np.int32)))
 
 
 def _attn_close(got, q, k, v, kpos, qpos, window, scale, what):
@@ -105,11 +105,11 @@ def test_masked_tail_of_full_cache_is_never_read(w4):
 def test_kv_append_ring_and_full_cache(w4, T, D, P):
     import torch
     kall, vall = synth.gen_attn_kv(940, P, D)
-    kr = torch.zeros((T, D), dtype=torch.int16, device="cuda")
-    vr = torch.zeros_like(kr)
-    kp = torch.full((T,), -1, dtype=torch.int32, device="cuda")
-    kf = torch.zeros_like(kr)
-    vf = torch.zeros_like(kr)
+    kr = gzeros((T, D), torch.int16)
+    vr = gzeros((T, D), torch.int16)
+    kp = gfull((T,), -1, torch.int32)
+    kf = gzeros((T, D), torch.int16)
+    vf = gzeros((T, D), torch.int16)
     pos = _i32(0)
     status = _i32(0)
     kro, vro, kpo = np.zeros((T, D), np.uint16), np.zeros((T, D), np.uint16), np.full(T, -1, np.int32)
@@ -161,7 +161,7 @@ def test_forced_lm_head(w4, N, K, group):
     assert gap > 2 * (1e-4 * ar[0, idx] + 1e-6), "ambiguous seed"
     assert a == idx
     # Forced: argmax = the forced token, y untouched.
-    yt = torch.full((1, N), 12345.0, dtype=torch.float32, device="cuda")
+    yt = gfull((1, N), 12345.0, torch.float32)
     forced.fill_(N - 3)
     _, a3 = w4.w4a16_gemv_argmax_forced(xd, qd, sd, forced, group=group, out=yt)
     torch.cuda.synchronize()
@@ -179,10 +179,10 @@ def test_prologue_bit_exact(w4, group):
     qt = synth.gen_qweight(960, V, K)
     sc = synth.gen_scales(960, V, K, group)
     qd, sd = to_dev_u32(qt), to_dev_bits16(sc)
-    tokens = torch.full((10,), -1, dtype=torch.int32, device="cuda")
+    tokens = gfull((10,), -1, torch.int32)
     hist = np.full(10, -1, np.int32)
     pos, status = _i32(5), _i32(0)
-    x = torch.empty((1, K), dtype=torch.bfloat16, device="cuda")
+    x = gempty((1, K), torch.bfloat16)
     cases = [(437, 0), (V, 1), (0, 0), (V - 1, 0), (-2, 1)]  # (token, expected new status bits)
     p = 5
     st_all = 0
@@ -230,22 +230,22 @@ def test_graph_replayed_decode_loop(w4, tied):
     eqd, esd = to_dev_u32(eq), to_dev_bits16(es)
     hqd, hsd = (eqd, esd) if tied else (to_dev_u32(hq), to_dev_bits16(hs))
     forced_d = torch.from_numpy(forced_seq).to(dev)
-    kr = torch.zeros((Tr, D), dtype=torch.int16, device=dev)
-    vr = torch.zeros_like(kr)
-    kpr = torch.full((Tr,), -1, dtype=torch.int32, device=dev)
-    kf = torch.zeros((Tf, D), dtype=torch.int16, device=dev)
-    vf = torch.zeros_like(kf)
-    pos = torch.zeros((1,), dtype=torch.int32, device=dev)
-    knew = torch.empty((D,), dtype=torch.int16, device=dev)
-    vnew = torch.empty_like(knew)
-    forced = torch.full((1,), -1, dtype=torch.int32, device=dev)
-    y = torch.empty((1, V), dtype=torch.float32, device=dev)
-    am = torch.empty((1,), dtype=torch.int32, device=dev)
-    tokens = torch.full((S + 1,), -1, dtype=torch.int32, device=dev)
-    status = torch.zeros((1,), dtype=torch.int32, device=dev)
-    att_r = torch.empty((H, D), dtype=torch.float32, device=dev)
-    att_f = torch.empty_like(att_r)
-    x = torch.empty((1, K), dtype=torch.bfloat16, device=dev)
+    kr = gzeros((Tr, D), torch.int16)
+    vr = gzeros((Tr, D), torch.int16)
+    kpr = gfull((Tr,), -1, torch.int32)
+    kf = gzeros((Tf, D), torch.int16)
+    vf = gzeros((Tf, D), torch.int16)
+    pos = gzeros((1,), torch.int32)
+    knew = gempty((D,), torch.int16)
+    vnew = gempty((D,), torch.int16)
+    forced = gfull((1,), -1, torch.int32)
+    y = gempty((1, V), torch.float32)
+    am = gempty((1,), torch.int32)
+    tokens = gfull((S + 1,), -1, torch.int32)
+    status = gzeros((1,), torch.int32)
+    att_r = gempty((H, D), torch.float32)
+    att_f = gempty((H, D), torch.float32)
+    x = gempty((1, K), torch.bfloat16)
     stream = torch.cuda.Stream()
 
     def step():
@@ -280,6 +280,7 @@ def test_graph_replayed_decode_loop(w4, tied):
             g.replay()
             hist_r[s].copy_(att_r); hist_f[s].copy_(att_f)
     torch.cuda.synchronize()
+    check_all("graph-replayed decode loop")
     got_tokens = tokens.cpu().numpy()
     got_r, got_f = hist_r.cpu().numpy(), hist_f.cpu().numpy()
     assert int(pos.item()) == S

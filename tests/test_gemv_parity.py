@@ -13,6 +13,7 @@ import pytest
 import oracle
 import synth
 from _util import assert_w4_close, to_dev_bits16, to_dev_u32
+from _guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +27,7 @@ def w4():
         pytest.skip("no GPU")
     import bit_weight_only_w4a16_gb300 as w4
     w4.init()
-    return w4
+    return guarded(w4)
 
 
 def _run(w4, x, qw, sc, argmax=False):

@@ -16,6 +16,7 @@ import pytest
 import oracle
 import synth
 from _util import assert_w4_close, bits16, to_dev_bits16
+from _guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -47,7 +48,7 @@ def table():
     torch.cuda.synchronize()
     rng = np.random.default_rng(55)
     rows = np.unique(np.concatenate([[0, 1, N // 2, N - 17, N - 16, N - 2, N - 1], rng.choice(N, 41, replace=False)]))
-    return w4, q, sc, rows
+    return guarded(w4), q, sc, rows
 
 
 @pytest.mark.parametrize("M", [1, 8])

@@ -15,6 +15,7 @@ import bench
 import oracle
 import synth
 from _util import assert_w4_close
+from _guard import Guard
 
 pytestmark = pytest.mark.gpu
 
@@ -44,6 +45,13 @@ def test_graph_replayed_sweep_sampled_rows(M):
     w4.init()
     dev = torch.device("cuda", 0)
     sweep = bench.Sweep(dev, keep_host=False, m=M)
+    # Each stage's y inside guard bands: a write past one stage's output would
+    # otherwise land unseen in the next stage's.
+    guards = []
+    for st in sweep.stages:
+        g = Guard((M, st["N"]), torch.float32, device=dev)
+        st["y"] = g.t
+        guards.append(g)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         sweep.run(w4, stream)
@@ -58,6 +66,8 @@ def test_graph_replayed_sweep_sampled_rows(M):
         g.replay()
     torch.cuda.synchronize()
     assert w4.device_error() == 0
+    for i, g in enumerate(guards):
+        g.check(f"sweep M={M} stage {i}")
     n = len(sweep.stages)
     picks = list(range(4)) + list(range(n - 4, n))  # every fused shape, layers 0 and 34
     rng = np.random.default_rng(1234 + M)
