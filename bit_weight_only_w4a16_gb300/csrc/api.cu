@@ -4,6 +4,7 @@
 #include "../../include/w4a16.h"
 #include "internal.h"
 
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -18,7 +19,8 @@ constexpr size_t kKeyCapacity = 8u * 65536u;
 constexpr size_t kWsFloats = 8u << 20;
 
 struct DeviceState {
-    bool ready = false;
+    // Set (release) once the fields below are written; read (acquire) first.
+    std::atomic<bool> ready{false};
     int num_sms = 0;
     unsigned long long *keys = nullptr;
     int *err = nullptr; // device error word written by kernels whose bounded waits ran out
@@ -49,12 +51,12 @@ int device_state(DeviceState **out)
     if (dev < 0 || dev >= kMaxDevices)
         return W4_ERR_NO_DEVICE;
     DeviceState &st = g_dev[dev];
-    if (st.ready) {
+    if (st.ready.load(std::memory_order_acquire)) {
         *out = &st;
         return W4_OK;
     }
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!st.ready) {
+    if (!st.ready.load(std::memory_order_relaxed)) {
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -79,7 +81,7 @@ int device_state(DeviceState **out)
             return cuda_fail(e);
         st.ws = static_cast<float *>(w);
         st.num_sms = sms;
-        st.ready = true;
+        st.ready.store(true, std::memory_order_release);
     }
     *out = &st;
     return W4_OK;

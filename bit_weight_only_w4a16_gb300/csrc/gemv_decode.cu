@@ -40,6 +40,9 @@
 namespace w4 {
 
 static constexpr int kTileK = 128; // k per tile of the m2 kernel: 4 groups
+// Shared memory two resident CTAs of the persistent forms may take together
+// (228 KB per SM, less 1 KB reserved per CTA and some headroom).
+static constexpr size_t kSmemPerSm = 220 * 1024;
 
 // xs[m * cpr + c] = permute_x8(x[m][8c .. 8c+7]) for m < rows, c < cpr (chunks
 // at or past K/8 are zero). Each thread issues up to kXLoads loads before it
@@ -1151,7 +1154,9 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
         p.ksplit = 1;
         p.warps = 8;
         p.unroll = 4;
-        p.grid = 2 * num_sms;
+        // Two resident CTAs per SM when both CTAs' x staging fits the SM's shared
+        // memory; one otherwise (the walk is the same for any grid).
+        p.grid = 2 * decode_smem_bytes(p, M, K) <= kSmemPerSm ? 2 * num_sms : num_sms;
         return p;
     }
     if (M <= 2) {
@@ -1230,7 +1235,7 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
             p.ksplit = 1;
             p.warps = 8;
             p.unroll = 4;
-            p.grid = 2 * num_sms;
+            p.grid = 2 * decode_smem_bytes(p, M, K) <= kSmemPerSm ? 2 * num_sms : num_sms;
             return p;
         }
         if (nrb >= 2 * num_sms && K % kTileK == 0) {

@@ -1,10 +1,9 @@
 // Decode GEMV with the fused greedy pick that allocates no device memory.
 //
-// Some callers cannot call cudaMalloc at all: code running inside a CUDA
-// graph that is being captured or replayed under a memory-pool policy that
-// forbids new allocations, plug-ins loaded into a host process that owns every
-// device allocation through its own allocator, and real-time decode loops that
-// must not hit the driver's allocator after start-up. For them this entry point
+// Some callers cannot call cudaMalloc at all: plug-ins loaded into a host
+// process that owns every device allocation through its own allocator, and
+// real-time decode loops that must not hit the driver's allocator after
+// start-up. For them this entry point
 // keeps its scratch (one 64-bit argmax key per CTA and x-row) in a fixed array
 // in the library's own device image instead of the scratch that w4_init
 // allocates.
@@ -21,6 +20,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 namespace {
@@ -31,7 +31,9 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned long long g_noalloc_keys[kNoallocKeys];
 
 struct NoallocDevice {
-    bool ready = false;
+    // Set (release) after keys and num_sms are written; read (acquire) before
+    // they are used, so a concurrent first call never sees a half-made state.
+    std::atomic<bool> ready{false};
     int num_sms = 0;
     unsigned long long *keys = nullptr; // device address of g_noalloc_keys
 };
@@ -50,9 +52,9 @@ int noalloc_device(NoallocDevice **out)
         return W4_ERR_NO_DEVICE;
     }
     NoallocDevice &d = g_na[dev];
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lk(g_na_mu);
-        if (!d.ready) {
+        if (!d.ready.load(std::memory_order_relaxed)) {
             int major = 0, minor = 0, sms = 0;
             if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
                 cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -70,7 +72,7 @@ int noalloc_device(NoallocDevice **out)
             }
             d.keys = ptr;
             d.num_sms = sms;
-            d.ready = true;
+            d.ready.store(true, std::memory_order_release);
         }
     }
     *out = &d;

@@ -121,17 +121,19 @@ int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32
                       const uint16_t *scales, int M, int N, int K, int group, void *stream);
 
 /*
- * w4a16_gemv_argmax for callers that cannot allocate device memory (inside a
- * CUDA graph under a no-new-allocation policy, a plug-in whose host owns every
- * device allocation, a real-time decode loop that must not reach the driver's
- * allocator). The pages have no counterpart; this is a library convenience.
+ * w4a16_gemv_argmax for callers that cannot allocate device memory: a plug-in
+ * loaded into a host process that owns every device allocation through its own
+ * allocator, or a real-time decode loop that must not reach the driver's
+ * allocator once it has started. The pages have no counterpart; this is a
+ * library convenience.
  * Same arguments, layouts, results and errors as w4a16_gemv_argmax, and it runs
  * the register-streaming decode kernels. It calls no cudaMalloc/cudaFree: its
  * scratch is a fixed 256 KiB array in the library's device image (held by every
  * GPU that loads the library until exit), with room for M * CTAs <= 32768 keys;
  * a larger call (about M * N / 128 > 32768) returns W4_ERR_UNSUPPORTED.
- * The first call on a device looks up the array's device address for that
- * device; make that first call before capturing this entry point in a stream.
+ * The first call on a device does a one-time set-up for that device (it looks
+ * up the array's device address, with that device current); make that first
+ * call before any stream capture begins.
  * All calls share the array: calls that overlap in time on the GPU (for
  * example on two streams) race on it and must be serialized by the caller.
  */

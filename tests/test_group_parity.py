@@ -15,6 +15,7 @@ import pytest
 import oracle
 import synth
 from _util import assert_w4_close, bits16, to_dev_bits16, to_dev_u32
+from _guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -28,7 +29,7 @@ def w4():
         pytest.skip("no GPU")
     import bit_weight_only_w4a16_gb300 as w4
     w4.init()
-    return w4
+    return guarded(w4)
 
 
 def _problem(seed, M, N, K, group):
@@ -82,6 +83,29 @@ def test_large_n_group256_argmax(w4, M):
         idx, gap = oracle.argmax(yfull[m])
         assert gap > 2 * (1e-4 * afull[m, idx] + 1e-6), "ambiguous seed"
         assert int(a.cpu().numpy()[m]) == idx
+
+
+@pytest.mark.parametrize("M,K,group", [(3, 8192, 64), (5, 8192, 128), (2, 32768, 32), (1, 8192, 256)])
+def test_large_n_long_k(w4, M, K, group):
+    """The persistent large-N forms where two CTAs' x staging no longer fits one
+    SM's shared memory (M * K * 2 bytes each): the planner runs one CTA per SM.
+    M = 3 and 5 take the M <= 8 form with one shared step per pair of groups
+    (group 64) and a shifted step index (group 128); M = 2 at K = 32768 the M <= 2
+    form. Sampled rows against the oracle; the pick equals the lowest index of
+    the largest logit the kernel wrote."""
+    import torch
+    N = 78000
+    x = synth.gen_x(800 + M, M, K)
+    sc = synth.gen_scales(801 + M, N, K, group)
+    q = synth.gen_qweight_torch(801 + M, N, K, torch.device("cuda"))
+    y, a = w4.w4a16_gemv_argmax(to_dev_bits16(x), q, to_dev_bits16(sc), group=group)
+    torch.cuda.synchronize()
+    y, a = y.cpu().numpy(), a.cpu().numpy()
+    rows = np.unique(np.concatenate([np.arange(0, N, 1013), [N - 17, N - 1]]))
+    yr, ar = oracle.gemm(x, synth.gen_qweight_rows(801 + M, N, K, rows), sc[rows], group)
+    assert_w4_close(y[:, rows], yr, ar, what=f"large N M{M} K{K} g{group}")
+    for m in range(M):
+        assert a[m] == int(np.argmax(y[m])), (m, a[m])
 
 
 @pytest.mark.parametrize("group", (64, 256, 512))

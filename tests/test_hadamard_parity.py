@@ -15,6 +15,7 @@ import pytest
 import oracle
 import synth
 from _util import assert_w4_close, to_dev_bits16, to_dev_u32
+from _guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +27,7 @@ def w4():
         pytest.skip("no GPU")
     import bit_weight_only_w4a16_gb300 as w4
     w4.init()
-    return w4
+    return guarded(w4)
 
 
 @pytest.mark.parametrize("M,N,K,b,group", [(1, 2560, 1536, 512, 32), (1, 1536, 6144, 256, 256),
@@ -48,7 +49,7 @@ def test_rotated_gemv_matches_oracle(w4, M, N, K, b, group):
     assert_w4_close(y.cpu().numpy(), yr, ar, what=f"hadamard M{M} N{N} K{K} b{b} g{group}")
 
 
-@pytest.mark.parametrize("M", [1, 2, 4])
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
 def test_rotated_lm_head_argmax(w4, M):
     """The vocabulary-projection forms (persistent kernels; at M = 2..4 the pair
     rows take the M <= 8 one) with the LM head's group 256 and the fused greedy

@@ -1,10 +1,15 @@
-"""The allocation-free argmax GEMV against the regular one (GPU).
+"""The allocation-free argmax GEMV against the regular one and the oracle (GPU).
 
-w4a16_gemv_argmax_noalloc serves callers that cannot allocate device memory;
-its scratch is a fixed array in the library's device image. It must give the
-same logits (within the GEMV tolerance) and the same greedy indices as
-w4a16_gemv_argmax, on consecutive calls that share that array. This file is
-collected last so a stop at the first failure has already run everything else.
+w4a16_gemv_argmax_noalloc serves callers that cannot allocate device memory (a
+plug-in whose host process owns every device allocation, a real-time decode
+loop that must not reach the driver's allocator after start-up); its scratch is
+a fixed array in the library's device image. It must give the same logits
+(within the GEMV tolerance) and the same greedy indices as w4a16_gemv_argmax,
+on consecutive calls that share that array; the logits must also meet the
+oracle's bound and the index must be the oracle's, and once the first call has
+done its per-device set-up, further calls must leave the device's free memory
+unchanged. This file is collected last so a stop at the first failure has
+already run everything else.
 """
 import ctypes
 
@@ -14,6 +19,7 @@ import pytest
 import oracle
 import synth
 from _util import assert_w4_close, to_dev_bits16, to_dev_u32
+from _guard import guarded
 
 pytestmark = pytest.mark.gpu
 
@@ -24,7 +30,7 @@ def w4():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     import bit_weight_only_w4a16_gb300 as w4
-    return w4
+    return guarded(w4)
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 20000, 1536), (2, 3001, 2048), (8, 5000, 1536)])
@@ -34,7 +40,7 @@ def test_noalloc_matches_regular_on_two_calls(w4, M, N, K):
     xd, qd, sd = to_dev_bits16(x), to_dev_u32(qw), to_dev_bits16(sc)
     y_ref, a_ref = w4.w4a16_gemv_argmax(xd, qd, sd)
     torch.cuda.synchronize()
-    _, absy = oracle.gemm(x, qw, sc)
+    y_or, absy = oracle.gemm(x, qw, sc)
     y_ref, a_ref = y_ref.cpu().numpy(), a_ref.cpu().numpy()
     for _ in range(2):
         y, a = w4.w4a16_gemv_argmax_noalloc(xd, qd, sd)
@@ -42,6 +48,41 @@ def test_noalloc_matches_regular_on_two_calls(w4, M, N, K):
         y, a = y.cpu().numpy(), a.cpu().numpy()
         assert_w4_close(y, y_ref.astype(np.float64), absy, what="noalloc vs regular")
         assert np.array_equal(a, a_ref)
+        # and against the oracle: the logits within the bound, the index exact
+        assert_w4_close(y, y_or, absy, what="noalloc vs oracle")
+        for m in range(M):
+            idx, gap = oracle.argmax(y_or[m])
+            assert gap > 2 * (1e-4 * absy[m, idx] + 1e-6), "ambiguous seed"
+            assert a[m] == idx, (m, a[m], idx)
+
+
+def test_noalloc_calls_leave_free_memory_unchanged(w4):
+    """After the first call (the per-device set-up), calls through the C ABI with
+    caller-owned buffers change the device's free memory by nothing."""
+    import torch
+    M, N, K = 1, 40000, 1536
+    x, qw, sc = synth.gen_w4_problem(4050, M, N, K)
+    xd, qd, sd = to_dev_bits16(x), to_dev_u32(qw), to_dev_bits16(sc)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    a = torch.empty((M,), dtype=torch.int32, device="cuda")
+    P = ctypes.c_void_p
+    lib = w4._lib
+
+    def call():
+        rc = lib.w4a16_gemv_argmax_noalloc(P(y.data_ptr()), P(a.data_ptr()), P(xd.data_ptr()), P(qd.data_ptr()),
+                                           P(sd.data_ptr()), M, N, K, 32, None)
+        assert rc == 0
+
+    call()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, (free0, free1)
+    y_or, _ = oracle.gemm(x, qw, sc)
+    assert int(a.item()) == oracle.argmax(y_or[0])[0]
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(w4):
