@@ -176,6 +176,10 @@ class ClockSampler:
         self.reader = threading.Thread(target=lambda: self.lines.extend(self.proc.stdout), daemon=True)
         self.reader.start()
 
+    def count(self) -> int:
+        """Samples received so far (None-safe when nvidia-smi is missing)."""
+        return len(self.lines) if self.proc is not None else -1
+
     def stop(self):
         if self.proc is None:
             return None
@@ -558,7 +562,7 @@ def captured_traffic():
     None when the decode kernel's sources changed after that capture."""
     import hashlib
     try:
-        with open(os.path.join(ROOT, "profiles", "gemv_m2_decode_sweep_traffic.json")) as f:
+        with open(os.path.join(ROOT, "profiles", "w4_decode_sweep_m1_35layers_traffic.json")) as f:
             rec = json.load(f)
         h = hashlib.sha256()
         for src in rec["sources"]:
@@ -624,20 +628,30 @@ def run_ours(args, rank, world):
             g.replay()
     torch.cuda.synchronize()
 
+    # The timed block of K steps is repeated (each block timed on its own with
+    # events) until the clock sampler holds >= 10 samples under load, so that
+    # the clock record stands on its own; the line reports the median block.
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(args.steps):
-            g.replay()
-        ev1.record(stream)
-    torch.cuda.synchronize()
+    block_ms = []
+    t_wall = time.time()
+    while True:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        block_ms.append(ev0.elapsed_time(ev1) / args.steps)
+        n_clk = clocks.count()
+        if n_clk < 0 or n_clk >= 10 or time.time() - t_wall > 20.0:
+            break
     barrier()
     clk = clocks.stop()
-    t_ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    t_ms = max_over_ranks(statistics.median(block_ms), world, dev)
     value = job_rate(t_ms, nbytes, world)
 
     # In-run read ceiling: the plain-sum probe over a 4 GiB buffer.
@@ -749,7 +763,9 @@ def run_ours(args, rank, world):
                      "kernel": "w4_decode_m1_kernel (q|k|v, o, down F=6144) and w4_decode_m2_kernel (gate|up, down F=12288): all 140 launches of the sweep"},
         "probe": {"hbm_read_probe_gbs": probe_gbs, "sweep_frac_of_probe": achieved / probe_gbs},
         "rows": rows,
-        "gpu_launches": ncalls * args.steps,
+        "gpu_launches": ncalls * args.steps * len(block_ms),
+        "timed_blocks": {"blocks": len(block_ms), "steps_per_block": args.steps,
+                         "ms_per_step_each": block_ms, "reported": "median block (max over ranks)"},
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -763,9 +779,14 @@ def run_ncu_case(case: str):
     """One small fixed case for an ncu capture: no timing, no output but "ok".
 
     decode_shapes : w4a16_gemv, M=1, twice on each of (24576,1536) (1536,12288)
-                    (2560,1536), writing a 256 MB buffer between calls.
-    m8_shapes     : the same shapes with M=8.
+                    (2560,1536) (1536,2048) (1536,6144), writing a 256 MB buffer
+                    between calls.
+    m8_shapes     : (24576,1536) (1536,12288) (2560,1536) with M=8.
     vocab         : w4a16_gemv_argmax twice on the 262144 x 1536 vocabulary projection.
+    m8_vocab      : the same with M=8 x-rows.
+    m8_ragged     : w4a16_gemv, M=8, twice on 4096 x 1056 (K not a multiple of 128:
+                    the 32-bit-load M <= 8 form).
+    Every case ends with hbm_read_probe over 1 GiB (the in-capture read ceiling).
     gather_probe  : w4_embed_gather of 8 ids from the 262144 x 8960 table and
                     hbm_read_probe over 1 GiB, twice each.
     attn          : w4_attn_decode twice over a 131072-slot x 512 cache (8 heads).
@@ -825,10 +846,16 @@ def run_ncu_case(case: str):
         v = torch.from_numpy(vh.view(np.int16)).to(dev)
         for _ in range(2):
             w4.w4_attn_decode(q, k, v, scale=D ** -0.5)
-    elif case == "vocab":
-        x, q, sc = problem(1000, 1, 262144, 1536)
+    elif case in ("vocab", "m8_vocab"):
+        x, q, sc = problem(1000, 1 if case == "vocab" else 8, 262144, 1536)
         for _ in range(2):
             w4.w4a16_gemv_argmax(x, q, sc)
+    elif case == "m8_ragged":
+        x, q, sc = problem(210, 8, 4096, 1056)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for rep in range(2):
+            flush.fill_(rep)
+            w4.w4a16_gemv(x, q, sc)
     elif case == "m8_shapes":
         data = [problem(200 + i, 8, N, K) for i, (N, K) in enumerate([(24576, 1536), (1536, 12288), (2560, 1536)])]
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -846,7 +873,8 @@ def run_ncu_case(case: str):
             w4.w4_embed_gather(ids, qt, st)
             w4.hbm_read_probe(buf)
     elif case == "decode_shapes":
-        data = [problem(100 + i, 1, N, K) for i, (N, K) in enumerate([(24576, 1536), (1536, 12288), (2560, 1536)])]
+        data = [problem(100 + i, 1, N, K) for i, (N, K) in
+                enumerate([(24576, 1536), (1536, 12288), (2560, 1536), (1536, 2048), (1536, 6144)])]
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         for rep in range(2):
             for x, q, sc in data:
@@ -859,6 +887,8 @@ def run_ncu_case(case: str):
             w4.w4a16_gemm(x, q, sc)
     else:
         raise SystemExit(f"unknown --ncu-case {case}")
+    probe = torch.ones(1 << 28, dtype=torch.int32, device=dev)
+    w4.hbm_read_probe(probe)
     torch.cuda.synchronize()
     print("ok")
 
