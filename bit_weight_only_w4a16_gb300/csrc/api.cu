@@ -170,6 +170,11 @@ int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int lg = w4::group_shift(group);
+    if (w4::vocab_supported(M, N, K, st->num_sms, lg, qweight, scales)) {
+        cudaError_t e = w4::run_decode_vocab(y, x, qweight, scales, N, K, lg, nullptr, nullptr, st->err,
+                                             st->num_sms, s);
+        return e == cudaSuccess ? W4_OK : cuda_fail(e);
+    }
     if (M == 1) {
         const w4::M1Plan mp = w4::plan_decode_m1(M, N, K, st->num_sms);
         if (mp.ok) {
@@ -222,6 +227,11 @@ int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int lg = w4::group_shift(group);
+    if (w4::vocab_supported(M, N, K, st->num_sms, lg, qweight, scales)) {
+        cudaError_t e = w4::run_decode_vocab(y, x, qweight, scales, N, K, lg, st->keys, argmax, st->err,
+                                             st->num_sms, s);
+        return e == cudaSuccess ? W4_OK : cuda_fail(e);
+    }
     const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
     if (!decode_fits(p, M, K) || (size_t)M * p.grid > kKeyCapacity)
         return W4_ERR_UNSUPPORTED;
@@ -408,6 +418,12 @@ int w4a16_gemv_argmax_forced(float *y, int32_t *argmax, const uint16_t *x, const
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
+    const int lg = w4::group_shift(group);
+    if (w4::vocab_supported(1, N, K, st->num_sms, lg, qweight, scales)) {
+        cudaError_t e = w4::run_decode_vocab(y, x, qweight, scales, N, K, lg, st->keys, argmax, st->err,
+                                             st->num_sms, static_cast<cudaStream_t>(stream), forced);
+        return e == cudaSuccess ? W4_OK : cuda_fail(e);
+    }
     const w4::DecodePlan p = w4::plan_decode(1, N, K, st->num_sms);
     if (p.kernel == 8 || !decode_fits(p, 1, K) || (size_t)p.grid > kKeyCapacity)
         return W4_ERR_UNSUPPORTED;

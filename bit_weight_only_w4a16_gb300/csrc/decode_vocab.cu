@@ -1,0 +1,388 @@
+// Vocabulary-sized decode GEMV (M = 1, optional fused greedy pick) with the
+// weights landed in shared memory by tensor copies.
+//
+// Source: "Gemma 4 E2B on a 4 GB GPU with pure PyTorch" - the w4gemv paragraph
+// (decode reads every weight once, straight from the packed 4-bit words, and
+// multiplies in registers without a 16-bit copy) and Step 2 (the tied 4-bit
+// embedding doubles as the output layer, read once per token with the greedy
+// pick).
+//
+// GB300 design. A 262144 x 1536 projection streams 226 MB with no dependency
+// chain inside, so what limits it is the bytes in flight per SM and the issue
+// rate. The register-preload form holds its in-flight tiles in registers (4
+// tiles a warp, 115 registers, 16 warps per SM: ~74 KB in flight). Here each
+// warp owns two shared-memory slots, each one half of a 16-row block (6 tiles
+// of 128 codes per row, 6 KB of codes), filled by ONE 3-D tensor copy issued by
+// the warp's lane 0 and completing on the slot's mbarrier. While the warp
+// computes one slot the other is in flight: 16 warps x 6 KB = 96 KB in flight
+// per SM, no registers held for it, and each tile costs the same instructions
+// as before with shared-memory loads (short, fixed latency) in place of
+// global ones.
+//
+// Layout. The copy box is {32 words, 3 chunks, 16 rows} with the hardware's
+// 128-byte swizzle: 16-byte granule q of 128-byte line L (L = 3 * row + chunk)
+// lands at granule q ^ (L & 7). A warp's 128-bit code load for one row is read
+// by 8 lanes at a time (rows of mma lanes g = 2p and 2p + 1, t = 0..3); mma row
+// g holds weight row perm(g) = (g >> 1) + 4 * (g & 1) (and + 8 for rows
+// g + 8), so the two rows of a phase are 4 apart, their lines 12 apart, and bit
+// 2 of L & 7 differs: the 8 lanes touch 8 different granules, all 32 banks
+// once.
+//
+// Inner product as in the other decode kernels: exact (code - 8) bf16 x bf16
+// m16n8k16 mma with fp32 accumulate; lane (g, t) holds group 4 * tile + t of
+// its two rows; B column s carries x restricted to group slot s; steps are
+// applied per (row, group) in fp32 (they come from global memory, one slot
+// ahead, since a steps row is not a multiple of 16 bytes for every group size).
+#include "common.cuh"
+#include "internal.h"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <type_traits>
+
+namespace w4 {
+
+namespace {
+
+constexpr int kTs = 6;                // tiles per slot (half a row block at K = 1536)
+constexpr int kLines = kTs / 2;       // 128-byte lines per row and slot
+constexpr int kSlotBytes = 16 * kTs * 64;
+constexpr int kStepBytes = 16 * kTs * 4 * 2; // group 32: 4 bf16 steps per tile and row
+constexpr int kWarps = 16;
+constexpr int kSlots = 2;             // per warp
+constexpr int kWaitLimit = 1 << 16;   // tests (each up to ~20 us) before a wait gives up
+constexpr int kDrainLimit = 64;       // tests per in-flight copy once a wait has given up
+
+struct VocabArgs {
+    float *y;
+    const uint16_t *x;
+    const uint16_t *sc;
+    unsigned long long *keys; // per-CTA argmax keys or null
+    int *err;                 // device error word: bit 0 set when a slot wait ran out
+    const int32_t *forced;    // forced next token (>= 0: no weight is read) or null
+    int N, K, lg;
+};
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+                 "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar,
+                                            uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+                 "l"(map), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ int perm_row(int g) { return (g >> 1) + 4 * (g & 1); }
+
+// Shared-memory byte offset of the 16 bytes of tile l (0..kTs-1), group slot t,
+// weight row r of a slot (swizzled as the copy lands it).
+__device__ __forceinline__ uint32_t code_off(int r, int l, int t)
+{
+    const int L = r * kLines + (l >> 1);
+    const int q = 4 * (l & 1) + t;
+    return (uint32_t)(L * 128 + ((q ^ (L & 7)) << 4));
+}
+
+// G32: the slot's steps arrive by a second tensor copy ({24 steps, 16 rows},
+// one 48-byte run per row) and are read from shared memory; other group sizes
+// (a steps row of K/group bf16 is not always a multiple of 16 bytes, which a
+// tensor copy needs) load theirs from global memory one slot ahead.
+template <bool ARGMAX, bool G32>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+w4_decode_vocab_kernel(const VocabArgs a, const __grid_constant__ CUtensorMap codes,
+                       const __grid_constant__ CUtensorMap steps)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) unsigned long long bars[kWarps * kSlots];
+    __shared__ unsigned long long ck;
+    __shared__ int s_abort;
+    // Slots on a 1024-byte boundary (the swizzle pattern's period).
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    if (ARGMAX && a.forced != nullptr && *a.forced >= 0) {
+        // The next token is forced: no weight is read, y is left as it was, and
+        // the pick kernel writes the forced token (after this grid completes).
+        pdl_launch_dependents();
+        pdl_wait();
+        return;
+    }
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int nrb = a.N >> 4;
+    const int T = a.K >> 7, halves = T / kTs;
+    const int GW = gridDim.x * kWarps, gw = blockIdx.x * kWarps + warp;
+    const int nmine = nrb > gw ? (nrb - gw + GW - 1) / GW : 0;
+    const int nslots = nmine * halves; // slot fills of this warp, in order
+
+    uint8_t *wslots = smem + (size_t)warp * kSlots * kSlotBytes;
+    const uint32_t wslot0 = smem_addr(wslots);
+    unsigned char *ssteps = smem + (size_t)kWarps * kSlots * kSlotBytes; // G32 steps slots
+    const uint32_t wstep0 = smem_addr(ssteps + (size_t)warp * kSlots * kStepBytes);
+    uint4 *xs = reinterpret_cast<uint4 *>(ssteps + (G32 ? (size_t)kWarps * kSlots * kStepBytes : 0));
+    const int nchunk = a.K >> 3;
+    uint4 *zs = xs + nchunk + 2;
+
+    const uint32_t bar0 = smem_addr(&bars[warp * kSlots]);
+    const uint64_t policy = policy_evict_first();
+    if (lane == 0) {
+        for (int i = 0; i < kSlots; ++i)
+            mbar_init(bar0 + 8u * i, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        ck = 0ull;
+    }
+    __syncwarp();
+
+    // Slot fill f (f = 0, 1, ...) of this warp: row block gw + (f / halves) * GW,
+    // half f % halves, into slot f % kSlots.
+    auto fill = [&](int f) {
+        const int rb = gw + (f / halves) * GW, h = f % halves;
+        const uint32_t bar = bar0 + 8u * (f % kSlots);
+        mbar_arrive_expect_tx(bar, (uint32_t)(kSlotBytes + (G32 ? kStepBytes : 0)));
+        tma_load_3d(wslot0 + (uint32_t)((f % kSlots) * kSlotBytes), &codes, 0, h * kLines, rb * 16, bar, policy);
+        if (G32)
+            tma_load_2d(wstep0 + (uint32_t)((f % kSlots) * kStepBytes), &steps, h * kTs * 4, rb * 16, bar, policy);
+    };
+    if (lane == 0)
+        for (int f = 0; f < kSlots && f < nslots; ++f)
+            fill(f);
+    if (threadIdx.x == 32)
+        prefetch_l2_bulk(a.x, (uint32_t)(a.K * 2));
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // x, permuted into the B-operand pair order; a zero region for the lanes
+    // that feed zero columns (granules on other banks than x's).
+    for (int i = threadIdx.x; i < nchunk; i += blockDim.x)
+        xs[i] = permute_x8(*reinterpret_cast<const uint4 *>(a.x + 8 * i));
+    if (threadIdx.x < 4)
+        zs[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+
+    const bool bsel = g < 4 && t == g;
+    const uint4 *xlane = bsel ? xs + 4 * t : zs;
+    const int xstep = bsel ? 16 : 0;
+
+    // This lane's weight rows in a row block and their step pointers.
+    const int rA = perm_row(g), rB = rA + 8;
+    const int sstride = (a.K >> 5) >> a.lg;
+    const int jt = 2 * (t & 1);
+    uint32_t sa[2][kTs], sb[2][kTs];
+    auto load_steps = [&](int f, auto bufc) {
+        constexpr int buf = decltype(bufc)::value;
+        if (G32)
+            return; // landed with the codes
+        const int rb = gw + (f / halves) * GW, h = f % halves;
+        const uint16_t *pa = a.sc + (size_t)(rb * 16 + rA) * sstride;
+        const uint16_t *pb = a.sc + (size_t)(rb * 16 + rB) * sstride;
+#pragma unroll
+        for (int l = 0; l < kTs; ++l) {
+            const int j = 4 * (h * kTs + l) + jt; // first 32-code group of the lane's pair
+            if (G32) {
+                sa[buf][l] = ldg_nc_u32(pa + j);
+                sb[buf][l] = ldg_nc_u32(pb + j);
+            } else {
+                sa[buf][l] = ldg_nc_u16(pa + (j >> a.lg));
+                sb[buf][l] = ldg_nc_u16(pb + (j >> a.lg));
+            }
+        }
+    };
+    if (nslots > 0)
+        load_steps(0, std::integral_constant<int, 0>{});
+
+    float accA = 0.f, accB = 0.f;
+    bool ok = true;         // warp-uniform: every slot wait so far completed
+    int issued = nslots < kSlots ? nslots : kSlots, failed = -1;
+    // One slot fill; BUF (compile-time) selects the step registers, so the two
+    // sets stay in registers (fills alternate between them).
+    auto consume = [&](auto bufc, int f) {
+        constexpr int buf = decltype(bufc)::value;
+        const uint32_t stA = wstep0 + (uint32_t)((f % kSlots) * kStepBytes + rA * kTs * 8 + 2 * jt);
+        const uint32_t stB = stA + 8u * 8u * kTs; // 8 rows on
+        if (f + 1 < nslots)
+            load_steps(f + 1, std::integral_constant<int, buf ^ 1>{});
+        const uint32_t bar = bar0 + 8u * (f % kSlots);
+        const uint32_t parity = (uint32_t)((f / kSlots) & 1);
+        if (ok) {
+            const bool done = mbar_wait_bounded(bar, parity, kWaitLimit);
+            ok = __all_sync(0xFFFFFFFFu, done);
+            if (!ok) {
+                failed = f;
+                if (lane == 0) {
+                    atomicOr(a.err, 1);
+                    s_abort = 1;
+                }
+            }
+        }
+        const uint32_t sbase = wslot0 + (uint32_t)((f % kSlots) * kSlotBytes);
+        const int h = f % halves;
+        const uint4 *xh = xlane + (size_t)xstep * h * kTs;
+#pragma unroll
+        for (int l = 0; l < kTs; l += 2) {
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, d0[4] = {0.f, 0.f, 0.f, 0.f};
+            float c1[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint4 wa0 = lds128(sbase + code_off(rA, l, t)), wb0 = lds128(sbase + code_off(rB, l, t));
+            const uint4 wa1 = lds128(sbase + code_off(rA, l + 1, t)), wb1 = lds128(sbase + code_off(rB, l + 1, t));
+            const uint4 *xb = xh + xstep * l;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 b0 = xb[i], b1 = xb[xstep + i];
+                unpack_mma2(c0, d0, (&wa0.x)[i], (&wb0.x)[i], b0.x, b0.y, b0.z, b0.w);
+                unpack_mma2(c1, d1, (&wa1.x)[i], (&wb1.x)[i], b1.x, b1.y, b1.z, b1.w);
+            }
+            if (G32) {
+                const uint32_t s0 = lds32(stA + 8u * l), s1 = lds32(stA + 8u * (l + 1));
+                const uint32_t t0 = lds32(stB + 8u * l), t1 = lds32(stB + 8u * (l + 1));
+                accA = fmaf(bf16lo_to_f32(s0), c0[0] + d0[0], accA);
+                accA = fmaf(bf16hi_to_f32(s0), c0[1] + d0[1], accA);
+                accB = fmaf(bf16lo_to_f32(t0), c0[2] + d0[2], accB);
+                accB = fmaf(bf16hi_to_f32(t0), c0[3] + d0[3], accB);
+                accA = fmaf(bf16lo_to_f32(s1), c1[0] + d1[0], accA);
+                accA = fmaf(bf16hi_to_f32(s1), c1[1] + d1[1], accA);
+                accB = fmaf(bf16lo_to_f32(t1), c1[2] + d1[2], accB);
+                accB = fmaf(bf16hi_to_f32(t1), c1[3] + d1[3], accB);
+            } else { // one step for both groups of the pair
+                accA = fmaf(bf16lo_to_f32(sa[buf][l]), (c0[0] + d0[0]) + (c0[1] + d0[1]), accA);
+                accB = fmaf(bf16lo_to_f32(sb[buf][l]), (c0[2] + d0[2]) + (c0[3] + d0[3]), accB);
+                accA = fmaf(bf16lo_to_f32(sa[buf][l + 1]), (c1[0] + d1[0]) + (c1[1] + d1[1]), accA);
+                accB = fmaf(bf16lo_to_f32(sb[buf][l + 1]), (c1[2] + d1[2]) + (c1[3] + d1[3]), accB);
+            }
+        }
+        // Every lane's reads of this slot are done (their values are in
+        // registers); lane 0 refills it with the warp's fill f + kSlots.
+        __syncwarp();
+        if (ok && f + kSlots < nslots) {
+            if (lane == 0)
+                fill(f + kSlots);
+            ++issued;
+        }
+        if (h == halves - 1) { // row block done: lanes t, t ^ 1 hold slots (0,1), (2,3)
+            const float vA = accA + __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
+            const float vB = accB + __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+            const int rb = gw + (f / halves) * GW;
+            if (t == 0) {
+                const int rowA = rb * 16 + rA, rowB = rb * 16 + rB;
+                a.y[rowA] = vA;
+                a.y[rowB] = vB;
+                if (ARGMAX) {
+                    atomicMax(&ck, argmax_key(vA, (uint32_t)rowA));
+                    atomicMax(&ck, argmax_key(vB, (uint32_t)rowB));
+                }
+            }
+            accA = accB = 0.f;
+        }
+    };
+    for (int f = 0; f < nslots; f += 2) {
+        consume(std::integral_constant<int, 0>{}, f);
+        if (f + 1 < nslots)
+            consume(std::integral_constant<int, 1>{}, f + 1);
+    }
+
+    // After a wait gave up: wait (bounded again) for this warp's copies still in
+    // flight, so none lands in shared memory after the CTA has exited.
+    if (failed >= 0 && lane == 0)
+        for (int f = failed; f < issued; ++f)
+            mbar_wait_bounded(bar0 + 8u * (f % kSlots), (uint32_t)((f / kSlots) & 1), kDrainLimit);
+
+    if (ARGMAX) {
+        __syncthreads();
+        if (threadIdx.x == 0)
+            a.keys[blockIdx.x] = ck;
+    }
+}
+
+constexpr size_t kSmem = (size_t)kWarps * kSlots * kSlotBytes; // + steps (group 32), x, zero region, slack
+
+} // namespace
+
+bool vocab_supported(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc)
+{
+    const int nrb = N / 16;
+    // Group 32 takes its steps by tensor copy (16-byte aligned steps); larger
+    // groups share one step per lane pair and load it from global memory.
+    // At least two slots per row block (K >= 1536): with one, a warp has too few
+    // fills to keep a copy in flight (80560 x 768 measured slower).
+    return M == 1 && K % (kTs * 128) == 0 && K >= 2 * kTs * 128 && N % 16 == 0 && nrb >= 2 * num_sms * kWarps &&
+           (reinterpret_cast<uintptr_t>(qw) & 15) == 0 && (lg > 0 || (reinterpret_cast<uintptr_t>(sc) & 15) == 0) &&
+           tmap_encoder() != nullptr &&
+           kSmem + (size_t)kWarps * kSlots * kStepBytes + (size_t)K * 2 + 64 + 1024 <= 226 * 1024;
+}
+
+cudaError_t run_decode_vocab(float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int N, int K,
+                             int lg, unsigned long long *keys, int32_t *argmax, int *err, int num_sms,
+                             cudaStream_t s, const int32_t *forced)
+{
+    auto enc = tmap_encoder();
+    if (!enc)
+        return cudaErrorNotSupported;
+    CUtensorMap map;
+    // codes as uint32 {32 words, K/256 chunks, N rows}; box {32, 3, 16}.
+    cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)N};
+    cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
+    cuuint32_t box[3] = {32, (cuuint32_t)kLines, 16};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    // steps (group 32) as uint16 {K/32, N}; box {24, 16}. Its row stride (K/16
+    // bytes) is a multiple of 16 since K % 768 == 0; vocab_supported checked
+    // that the base is 16-byte aligned.
+    CUtensorMap smap = map;
+    const bool g32_tma = lg == 0;
+    if (g32_tma) {
+        cuuint64_t sd[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
+        cuuint64_t ss[1] = {(cuuint64_t)K / 16};
+        cuuint32_t sbx[2] = {(cuuint32_t)(kTs * 4), 16};
+        cuuint32_t ses[2] = {1, 1};
+        if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(sc), sd, ss, sbx, ses,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    VocabArgs a;
+    a.y = y;
+    a.x = x;
+    a.sc = sc;
+    a.keys = keys;
+    a.err = err;
+    a.forced = argmax != nullptr ? forced : nullptr;
+    a.N = N;
+    a.K = K;
+    a.lg = lg;
+    const size_t smem = kSmem + (g32_tma ? (size_t)kWarps * kSlots * kStepBytes : 0) + (size_t)(K / 8 + 8) * 16 + 1024;
+    const bool am = argmax != nullptr;
+    auto kern = am ? (g32_tma ? w4_decode_vocab_kernel<true, true> : w4_decode_vocab_kernel<true, false>)
+                   : (g32_tma ? w4_decode_vocab_kernel<false, true> : w4_decode_vocab_kernel<false, false>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, map, smap);
+    if (e != cudaSuccess || !am)
+        return e;
+    return run_argmax_finalize(argmax, keys, 1, num_sms, s, a.forced);
+}
+
+} // namespace w4

@@ -432,24 +432,9 @@ prefill_split_reduce_kernel(float *__restrict__ y, const float *__restrict__ ws,
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encoder()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void *p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 cudaError_t launch(const PrefillArgs &a, const uint16_t *x, int grid, cudaStream_t s)
 {
-    auto enc = encoder();
+    auto enc = tmap_encoder();
     if (!enc)
         return cudaErrorNotSupported;
     CUtensorMap xmap;
@@ -515,6 +500,21 @@ PrefillPlan plan_prefill(int M, int N, int K, int num_sms, size_t ws_floats)
     p.bn = kBN;
     p.ok = true;
     return p;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
 }
 
 cudaError_t run_prefill(const PrefillPlan &p, float *y, const uint16_t *x, const uint32_t *qw,

@@ -3,6 +3,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 namespace w4 {
@@ -56,6 +58,21 @@ struct M1Plan {
 M1Plan plan_decode_m1(int M, int N, int K, int num_sms);
 cudaError_t run_decode_m1(const M1Plan &p, float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc,
                           int N, int K, int lg, cudaStream_t s);
+
+// The driver's cuTensorMapEncodeTiled (looked up once), or null.
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder();
+
+// Vocabulary-sized M = 1 decode GEMV with the weights landed in shared memory by
+// tensor copies (K % 768 == 0, K >= 1536, N % 16 == 0, at least two 16-row blocks per warp
+// of a full wave, 16-byte aligned codes, and 16-byte aligned steps at group 32). With argmax != nullptr the per-CTA
+// keys go to keys[0 .. num_sms) and argmax[0] receives the pick. A slot wait
+// that runs out sets bit 0 of *err.
+bool vocab_supported(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc);
+// forced (with argmax): when *forced >= 0 as the kernel starts, no weight is
+// read, y is left as it was and argmax[0] = *forced.
+cudaError_t run_decode_vocab(float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int N, int K,
+                             int lg, unsigned long long *keys, int32_t *argmax, int *err, int num_sms,
+                             cudaStream_t s, const int32_t *forced = nullptr);
 
 // argmax[m] = index of the largest key in keys[m][0 .. nblocks), or *forced
 // when forced != nullptr and *forced >= 0.
