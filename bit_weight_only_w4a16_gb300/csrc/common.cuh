@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace w4 {
@@ -272,6 +273,61 @@ __device__ __forceinline__ void unpack_mma2(float (&c)[4], float (&d)[4], uint32
         "}\n"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3]), "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(wa), "r"(wb), "r"(x0), "r"(x1), "r"(x2), "r"(x3));
+}
+
+// The fp16 form of unpack_mma2, for x rows held in fp16 (exactly: see
+// bf16x2_to_f16x2_exact). In fp16 a nibble fits the 10-bit mantissa at bits
+// 0..3 and at bits 4..7 of each half, so one shift per word serves four pairs:
+// (w & 0x000F000F) | 0x6400 halves are 1024 + c (minus 1032 leaves c - 8) and
+// (w & 0x00F000F0) | 0x6400 halves are 1024 + 16 c (times 1/16 minus 72 leaves
+// c - 8); both exact in fp16. Per word: 1 shift + 4 lop3 on the ALU pipe
+// (against 3 + 4 in the bf16 form) and 2 sub + 2 fma on the FMA pipe.
+__device__ __forceinline__ void unpack_mma2_f16(float (&c)[4], float (&d)[4], uint32_t wa, uint32_t wb,
+                                                uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3)
+{
+    asm("{\n"
+        ".reg .b32 p0, p1, p2, p3, q0, q1, q2, q3, t, u, ml, mh, o, k, s, b;\n"
+        "mov.b32 ml, 0x000F000F;\n"
+        "mov.b32 mh, 0x00F000F0;\n"
+        "mov.b32 o, 0x64006400;\n"
+        "mov.b32 k, 0x64086408;\n"
+        "mov.b32 s, 0x2C002C00;\n"
+        "mov.b32 b, 0xD480D480;\n"
+        "lop3.b32 p0, %8, ml, o, 0xEA;\n"
+        "lop3.b32 p1, %8, mh, o, 0xEA;\n"
+        "shr.u32 t, %8, 8;\n"
+        "lop3.b32 p2, t, ml, o, 0xEA;\n"
+        "lop3.b32 p3, t, mh, o, 0xEA;\n"
+        "lop3.b32 q0, %9, ml, o, 0xEA;\n"
+        "lop3.b32 q1, %9, mh, o, 0xEA;\n"
+        "shr.u32 u, %9, 8;\n"
+        "lop3.b32 q2, u, ml, o, 0xEA;\n"
+        "lop3.b32 q3, u, mh, o, 0xEA;\n"
+        "sub.rn.f16x2 p0, p0, k;\n fma.rn.f16x2 p1, p1, s, b;\n sub.rn.f16x2 p2, p2, k;\n fma.rn.f16x2 p3, p3, s, b;\n"
+        "sub.rn.f16x2 q0, q0, k;\n fma.rn.f16x2 q1, q1, s, b;\n sub.rn.f16x2 q2, q2, k;\n fma.rn.f16x2 q3, q3, s, b;\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {p0,q0,p1,q1}, {%10,%11}, {%0,%1,%2,%3};\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%4,%5,%6,%7}, {p2,q2,p3,q3}, {%12,%13}, {%4,%5,%6,%7};\n"
+        "}\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3]), "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(wa), "r"(wb), "r"(x0), "r"(x1), "r"(x2), "r"(x3));
+}
+
+// Two bf16 values (low half first) as two fp16 values, and whether both are
+// exact there: zero, or an exponent in [-17, 15] (8 significant bits then fit
+// fp16's normal range or its subnormal grid of 2^-24). Other values (larger,
+// smaller, bf16 subnormals, inf, NaN) clear ok.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_exact(uint32_t u, bool &ok)
+{
+    uint32_t r = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t b = (u >> (16 * h)) & 0xFFFFu;
+        const uint32_t e = (b >> 7) & 0xFFu;
+        ok = ok && ((b & 0x7FFFu) == 0 || (e >= 110u && e <= 142u));
+        const __half v = __float2half_rn(__uint_as_float(b << 16));
+        r |= (uint32_t)__half_as_ushort(v) << (16 * h);
+    }
+    return r;
 }
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t u) { return __uint_as_float(u << 16); }

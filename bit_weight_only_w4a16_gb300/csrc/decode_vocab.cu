@@ -164,9 +164,27 @@ w4_decode_vocab_kernel(const VocabArgs a, const __grid_constant__ CUtensorMap co
     pdl_wait();
 
     // x, permuted into the B-operand pair order; a zero region for the lanes
-    // that feed zero columns (granules on other banks than x's).
-    for (int i = threadIdx.x; i < nchunk; i += blockDim.x)
-        xs[i] = permute_x8(*reinterpret_cast<const uint4 *>(a.x + 8 * i));
+    // that feed zero columns (granules on other banks than x's). When every x
+    // value is exact in fp16 the CTA runs the fp16 unpack (fewer ALU
+    // instructions per code; the same products and fp32 sums), else the bf16 one.
+    bool exact = true;
+    for (int i = threadIdx.x; i < nchunk; i += blockDim.x) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(a.x + 8 * i);
+        bf16x2_to_f16x2_exact(v.x, exact);
+        bf16x2_to_f16x2_exact(v.y, exact);
+        bf16x2_to_f16x2_exact(v.z, exact);
+        bf16x2_to_f16x2_exact(v.w, exact);
+    }
+    const bool f16 = __syncthreads_and(exact) != 0;
+    for (int i = threadIdx.x; i < nchunk; i += blockDim.x) {
+        uint4 v = *reinterpret_cast<const uint4 *>(a.x + 8 * i);
+        if (f16) {
+            bool dummy = true;
+            v = make_uint4(bf16x2_to_f16x2_exact(v.x, dummy), bf16x2_to_f16x2_exact(v.y, dummy),
+                           bf16x2_to_f16x2_exact(v.z, dummy), bf16x2_to_f16x2_exact(v.w, dummy));
+        }
+        xs[i] = permute_x8(v);
+    }
     if (threadIdx.x < 4)
         zs[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
@@ -207,8 +225,9 @@ w4_decode_vocab_kernel(const VocabArgs a, const __grid_constant__ CUtensorMap co
     int issued = nslots < kSlots ? nslots : kSlots, failed = -1;
     // One slot fill; BUF (compile-time) selects the step registers, so the two
     // sets stay in registers (fills alternate between them).
-    auto consume = [&](auto bufc, int f) {
+    auto consume = [&](auto bufc, auto f16c, int f) {
         constexpr int buf = decltype(bufc)::value;
+        constexpr bool F16 = decltype(f16c)::value;
         const uint32_t stA = wstep0 + (uint32_t)((f % kSlots) * kStepBytes + rA * kTs * 8 + 2 * jt);
         const uint32_t stB = stA + 8u * 8u * kTs; // 8 rows on
         if (f + 1 < nslots)
@@ -239,8 +258,13 @@ w4_decode_vocab_kernel(const VocabArgs a, const __grid_constant__ CUtensorMap co
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 b0 = xb[i], b1 = xb[xstep + i];
-                unpack_mma2(c0, d0, (&wa0.x)[i], (&wb0.x)[i], b0.x, b0.y, b0.z, b0.w);
-                unpack_mma2(c1, d1, (&wa1.x)[i], (&wb1.x)[i], b1.x, b1.y, b1.z, b1.w);
+                if (F16) {
+                    unpack_mma2_f16(c0, d0, (&wa0.x)[i], (&wb0.x)[i], b0.x, b0.y, b0.z, b0.w);
+                    unpack_mma2_f16(c1, d1, (&wa1.x)[i], (&wb1.x)[i], b1.x, b1.y, b1.z, b1.w);
+                } else {
+                    unpack_mma2(c0, d0, (&wa0.x)[i], (&wb0.x)[i], b0.x, b0.y, b0.z, b0.w);
+                    unpack_mma2(c1, d1, (&wa1.x)[i], (&wb1.x)[i], b1.x, b1.y, b1.z, b1.w);
+                }
             }
             if (G32) {
                 const uint32_t s0 = lds32(stA + 8u * l), s1 = lds32(stA + 8u * (l + 1));
@@ -284,11 +308,17 @@ w4_decode_vocab_kernel(const VocabArgs a, const __grid_constant__ CUtensorMap co
             accA = accB = 0.f;
         }
     };
-    for (int f = 0; f < nslots; f += 2) {
-        consume(std::integral_constant<int, 0>{}, f);
-        if (f + 1 < nslots)
-            consume(std::integral_constant<int, 1>{}, f + 1);
-    }
+    auto run = [&](auto f16c) {
+        for (int f = 0; f < nslots; f += 2) {
+            consume(std::integral_constant<int, 0>{}, f16c, f);
+            if (f + 1 < nslots)
+                consume(std::integral_constant<int, 1>{}, f16c, f + 1);
+        }
+    };
+    if (f16)
+        run(std::true_type{});
+    else
+        run(std::false_type{});
 
     // After a wait gave up: wait (bounded again) for this warp's copies still in
     // flight, so none lands in shared memory after the CTA has exited.

@@ -196,6 +196,36 @@ def test_vocab_projection_with_argmax(w4):
     assert int(a[0]) == int(np.argmax(y[0]))
 
 
+@pytest.mark.parametrize("special", ["none", "large", "tiny", "subnormal", "zeros"])
+@pytest.mark.parametrize("N,K,group", [(262144, 1536, 32), (131072, 3072, 256), (80000, 1536, 32)])
+def test_fp16_and_bf16_unpack_forms(w4, special, N, K, group):
+    """The kernels run an fp16 unpack when every x value is exact in fp16 and
+    the bf16 one otherwise. x values outside fp16's exact range (2^20, 2^-30, a
+    bf16 subnormal) force the bf16 form; x with exact zeros keeps the fp16 one.
+    Both must meet the bound on sampled rows, and the pick must be the lowest
+    index of the largest logit written."""
+    import torch
+    seed = 1300 + K + group
+    x = synth.gen_x(seed, 1, K).copy()
+    if special == "large":
+        x[0, 17] = 0x4980          # 2^20: beyond fp16's range
+    elif special == "tiny":
+        x[0, 300] = 0x3080         # 2^-30: below fp16's subnormal grid
+    elif special == "subnormal":
+        x[0, 5] = 0x0001           # a bf16 subnormal
+    elif special == "zeros":
+        x[0, 64:96] = 0x0000
+    qd = synth.gen_qweight_torch(seed, N, K, "cuda")
+    sc = synth.gen_scales(seed, N, K, group)
+    y, a = w4.w4a16_gemv_argmax(to_dev_bits16(x), qd, to_dev_bits16(sc), group=group)
+    torch.cuda.synchronize()
+    y, a = y.cpu().numpy(), a.cpu().numpy()
+    rows = np.unique(np.concatenate([[0, N - 1], np.arange(7, N, 4099)]))
+    yr, ar = oracle.gemm(x, synth.gen_qweight_rows(seed, N, K, rows), sc[rows], group)
+    assert_w4_close(y[:, rows], yr, ar, what=f"x {special} {N}x{K} g{group}")
+    assert int(a[0]) == int(np.argmax(y[0]))
+
+
 @pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
 def test_large_n_sampled_rows_and_argmax(w4, M):
     # N = 80000 (5000 row blocks: the persistent large-N forms on a 152-SM GPU,
