@@ -181,6 +181,11 @@ int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
             cudaError_t e = w4::run_decode_m1(mp, y, x, qweight, scales, N, K, lg, s);
             return e == cudaSuccess ? W4_OK : cuda_fail(e);
         }
+        const int R = w4::slab_rows_per_cta(M, N, K, st->num_sms, lg, qweight, scales);
+        if (R > 0) {
+            cudaError_t e = w4::run_decode_slab(R, y, x, qweight, scales, N, K, st->err, s);
+            return e == cudaSuccess ? W4_OK : cuda_fail(e);
+        }
     }
     const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
     if (!decode_fits(p, M, K))

@@ -335,6 +335,155 @@ w4_decode_vocab_kernel(const VocabArgs a, const __grid_constant__ CUtensorMap co
 
 constexpr size_t kSmem = (size_t)kWarps * kSlots * kSlotBytes; // + steps (group 32), x, zero region, slack
 
+// The decode sweep's long M = 1 projections (gate|up, down) with the same
+// shared-memory slots: a CTA owns R consecutive 16-row blocks and all S = T/6
+// six-tile slices of them ("units", R * S of them); warp w of W (16, or 8 when
+// 16 warps' slots and x do not fit) takes units w, w + W, ... into its two
+// slots. The slots' copies are issued when the CTA starts, before the wait on
+// the previous call, so a CTA whose units fit its 2 W slots has its whole
+// weight slice requested at once. After the wait x is
+// staged, each warp computes its units from shared memory and leaves each
+// unit's 16 row partials in shared memory; the partials of a row are added in
+// slice order (deterministic). Group 32 only (steps by tensor copy).
+__global__ void __launch_bounds__(kWarps * 32, 1)
+w4_decode_slab_kernel(const VocabArgs a, int R, const __grid_constant__ CUtensorMap codes,
+                      const __grid_constant__ CUtensorMap steps)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) unsigned long long bars[kWarps * kSlots];
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int W = blockDim.x >> 5; // 16 warps, or 8 when 16 warps' slots and x do not fit
+    const int g = lane >> 2, t = lane & 3;
+    const int nrb = a.N >> 4;
+    const int S = (a.K >> 7) / kTs;                 // six-tile slices per row
+    const int rb0 = blockIdx.x * R;
+    const int Rn = min(R, nrb - rb0);
+    const int nunits = Rn * S;
+    const int nmine = warp < nunits ? (nunits - warp + W - 1) / W : 0;
+
+    const uint32_t wslot0 = smem_addr(smem + (size_t)warp * kSlots * kSlotBytes);
+    unsigned char *ssteps = smem + (size_t)W * kSlots * kSlotBytes;
+    const uint32_t wstep0 = smem_addr(ssteps + (size_t)warp * kSlots * kStepBytes);
+    uint4 *xs = reinterpret_cast<uint4 *>(ssteps + (size_t)W * kSlots * kStepBytes);
+    const int nchunk = a.K >> 3;
+    uint4 *zs = xs + nchunk + 2;
+    float *red = reinterpret_cast<float *>(zs + 6); // [nunits][16]
+
+    const uint32_t bar0 = smem_addr(&bars[warp * kSlots]);
+    const uint64_t policy = policy_evict_first();
+    if (lane == 0) {
+        for (int i = 0; i < kSlots; ++i)
+            mbar_init(bar0 + 8u * i, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    // Fill f of this warp: unit warp + f * W = (row block r, slice h).
+    auto fill = [&](int f) {
+        const int u = warp + f * W, r = u / S, h = u - r * S;
+        const uint32_t bar = bar0 + 8u * (f % kSlots);
+        mbar_arrive_expect_tx(bar, (uint32_t)(kSlotBytes + kStepBytes));
+        tma_load_3d(wslot0 + (uint32_t)((f % kSlots) * kSlotBytes), &codes, 0, h * kLines, (rb0 + r) * 16, bar,
+                    policy);
+        tma_load_2d(wstep0 + (uint32_t)((f % kSlots) * kStepBytes), &steps, h * kTs * 4, (rb0 + r) * 16, bar,
+                    policy);
+    };
+    if (lane == 0)
+        for (int f = 0; f < kSlots && f < nmine; ++f)
+            fill(f);
+    if (threadIdx.x == 32)
+        prefetch_l2_bulk(a.x, (uint32_t)(a.K * 2));
+    pdl_launch_dependents();
+    pdl_wait();
+
+    for (int i = threadIdx.x; i < nchunk; i += blockDim.x)
+        xs[i] = permute_x8(*reinterpret_cast<const uint4 *>(a.x + 8 * i));
+    if (threadIdx.x < 4)
+        zs[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+
+    const bool bsel = g < 4 && t == g;
+    const uint4 *xlane = bsel ? xs + 4 * t : zs;
+    const int xstep = bsel ? 16 : 0;
+    const int rA = perm_row(g), rB = rA + 8;
+    const int jt = 2 * (t & 1);
+
+    bool ok = true;
+    int issued = nmine < kSlots ? nmine : kSlots, failed = -1;
+    for (int f = 0; f < nmine; ++f) {
+        const uint32_t bar = bar0 + 8u * (f % kSlots);
+        const uint32_t parity = (uint32_t)((f / kSlots) & 1);
+        if (ok) {
+            const bool done = mbar_wait_bounded(bar, parity, kWaitLimit);
+            ok = __all_sync(0xFFFFFFFFu, done);
+            if (!ok) {
+                failed = f;
+                if (lane == 0)
+                    atomicOr(a.err, 1);
+            }
+        }
+        const int u = warp + f * W, h = u % S;
+        const uint32_t sbase = wslot0 + (uint32_t)((f % kSlots) * kSlotBytes);
+        const uint32_t stA = wstep0 + (uint32_t)((f % kSlots) * kStepBytes + rA * kTs * 8 + 2 * jt);
+        const uint32_t stB = stA + 8u * 8u * kTs;
+        const uint4 *xh = xlane + (size_t)xstep * h * kTs;
+        float accA = 0.f, accB = 0.f;
+#pragma unroll
+        for (int l = 0; l < kTs; l += 2) {
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, d0[4] = {0.f, 0.f, 0.f, 0.f};
+            float c1[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint4 wa0 = lds128(sbase + code_off(rA, l, t)), wb0 = lds128(sbase + code_off(rB, l, t));
+            const uint4 wa1 = lds128(sbase + code_off(rA, l + 1, t)), wb1 = lds128(sbase + code_off(rB, l + 1, t));
+            const uint4 *xb = xh + xstep * l;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 b0 = xb[i], b1 = xb[xstep + i];
+                unpack_mma2(c0, d0, (&wa0.x)[i], (&wb0.x)[i], b0.x, b0.y, b0.z, b0.w);
+                unpack_mma2(c1, d1, (&wa1.x)[i], (&wb1.x)[i], b1.x, b1.y, b1.z, b1.w);
+            }
+            const uint32_t s0 = lds32(stA + 8u * l), s1 = lds32(stA + 8u * (l + 1));
+            const uint32_t t0 = lds32(stB + 8u * l), t1 = lds32(stB + 8u * (l + 1));
+            accA = fmaf(bf16lo_to_f32(s0), c0[0] + d0[0], accA);
+            accA = fmaf(bf16hi_to_f32(s0), c0[1] + d0[1], accA);
+            accB = fmaf(bf16lo_to_f32(t0), c0[2] + d0[2], accB);
+            accB = fmaf(bf16hi_to_f32(t0), c0[3] + d0[3], accB);
+            accA = fmaf(bf16lo_to_f32(s1), c1[0] + d1[0], accA);
+            accA = fmaf(bf16hi_to_f32(s1), c1[1] + d1[1], accA);
+            accB = fmaf(bf16lo_to_f32(t1), c1[2] + d1[2], accB);
+            accB = fmaf(bf16hi_to_f32(t1), c1[3] + d1[3], accB);
+        }
+        __syncwarp();
+        if (ok && f + kSlots < nmine) {
+            if (lane == 0)
+                fill(f + kSlots);
+            ++issued;
+        }
+        // Lanes t, t ^ 1 hold group slots (0, 1) and (2, 3) of the unit's rows.
+        const float vA = accA + __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
+        const float vB = accB + __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+        if (t == 0) {
+            red[u * 16 + rA] = vA;
+            red[u * 16 + rB] = vB;
+        }
+    }
+    if (failed >= 0 && lane == 0)
+        for (int f = failed; f < issued; ++f)
+            mbar_wait_bounded(bar0 + 8u * (f % kSlots), (uint32_t)((f / kSlots) & 1), kDrainLimit);
+    __syncthreads();
+
+    // Each row's slices, added in slice order.
+    float *yb = a.y + (size_t)rb0 * 16;
+    for (int o = threadIdx.x; o < Rn * 16; o += blockDim.x) {
+        const float *p = red + (o >> 4) * S * 16 + (o & 15);
+        float v = p[0];
+        for (int h = 1; h < S; ++h)
+            v += p[16 * h];
+        yb[o] = v;
+    }
+}
+
+
 } // namespace
 
 bool vocab_supported(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc)
@@ -413,6 +562,94 @@ cudaError_t run_decode_vocab(float *y, const uint16_t *x, const uint32_t *qw, co
     if (e != cudaSuccess || !am)
         return e;
     return run_argmax_finalize(argmax, keys, 1, num_sms, s, a.forced);
+}
+
+// Shared memory of the slab form for W warps, and the warp count it launches
+// with: 16 when that fits (and the units fill the slots), else 8; 0 if neither
+// holds every unit within the slots.
+static size_t slab_smem(int W, int R, int S, int K)
+{
+    return (size_t)W * kSlots * (kSlotBytes + kStepBytes) + (size_t)(K / 8 + 8) * 16 + (size_t)R * S * 16 * 4 + 1024;
+}
+
+static int slab_warps(int R, int S, int K)
+{
+    for (int W = kWarps; W >= 8; W /= 2)
+        if (R * S <= W * kSlots && slab_smem(W, R, S, K) <= 226 * 1024)
+            return W;
+    return 0;
+}
+
+// Row blocks per CTA of the slab form and whether it serves (N, K): group 32,
+// K % 768 == 0, N % 16 == 0, 16-byte aligned codes and steps, a CTA's units
+// within its 32 slots (so every copy is issued before the dependency wait),
+// below vocabulary sizes.
+int slab_rows_per_cta(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc)
+{
+    if (M != 1 || lg != 0 || K % (kTs * 128) != 0 || N % 16 != 0 || num_sms < 1)
+        return 0;
+    if ((reinterpret_cast<uintptr_t>(qw) & 15) != 0 || (reinterpret_cast<uintptr_t>(sc) & 15) != 0 ||
+        tmap_encoder() == nullptr)
+        return 0;
+    const int nrb = N / 16, S = K / (kTs * 128);
+    const int R = (nrb + num_sms - 1) / num_sms;
+    if (nrb >= 2 * num_sms * kWarps || slab_warps(R, S, K) == 0)
+        return 0;
+    return R;
+}
+
+cudaError_t run_decode_slab(int R, float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int N,
+                            int K, int *err, cudaStream_t s)
+{
+    auto enc = tmap_encoder();
+    if (!enc || R < 1)
+        return cudaErrorNotSupported;
+    CUtensorMap map, smap;
+    cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)N};
+    cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
+    cuuint32_t box[3] = {32, (cuuint32_t)kLines, 16};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cuuint64_t sd[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
+    cuuint64_t ss[1] = {(cuuint64_t)K / 16};
+    cuuint32_t sbx[2] = {(cuuint32_t)(kTs * 4), 16};
+    cuuint32_t ses[2] = {1, 1};
+    if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(sc), sd, ss, sbx, ses,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    VocabArgs a;
+    a.y = y;
+    a.x = x;
+    a.sc = sc;
+    a.keys = nullptr;
+    a.err = err;
+    a.forced = nullptr;
+    a.N = N;
+    a.K = K;
+    a.lg = 0;
+    const int S = K / (kTs * 128), nrb = N / 16;
+    const int W = slab_warps(R, S, K);
+    if (W == 0)
+        return cudaErrorNotSupported;
+    const size_t smem = slab_smem(W, R, S, K);
+    cudaError_t e = cudaFuncSetAttribute(w4_decode_slab_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((nrb + R - 1) / R);
+    cfg.blockDim = dim3(W * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, w4_decode_slab_kernel, a, R, map, smap);
 }
 
 } // namespace w4

@@ -74,6 +74,13 @@ cudaError_t run_decode_vocab(float *y, const uint16_t *x, const uint32_t *qw, co
                              int lg, unsigned long long *keys, int32_t *argmax, int *err, int num_sms,
                              cudaStream_t s, const int32_t *forced = nullptr);
 
+// The decode sweep's long M = 1 projections with the same shared-memory slots:
+// rows per CTA when the form serves (N, K) (group 32, K % 768 == 0, N % 16 == 0,
+// 16-byte aligned codes and steps, a CTA's slices within its slots), else 0.
+int slab_rows_per_cta(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc);
+cudaError_t run_decode_slab(int R, float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int N,
+                            int K, int *err, cudaStream_t s);
+
 // argmax[m] = index of the largest key in keys[m][0 .. nblocks), or *forced
 // when forced != nullptr and *forced >= 0.
 cudaError_t run_argmax_finalize(int32_t *argmax, const unsigned long long *keys, int M, int nblocks,
