@@ -380,6 +380,14 @@ def measure_rows(w4, dev, stream, sweep=None):
     us = graph_time(lambda: w4.w4a16_gemv_argmax(x, q, sc, out=y, argmax=am, stream=stream), reps=10)
     b = stage_bytes(N, K) + 4
     res["vocab_argmax_262144x1536"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    # The same projection for 8 x-rows (8 sequences), a pick per x-row.
+    x8 = dev16(synth.gen_x(1001, 8, K))
+    y8 = torch.empty((8, N), dtype=torch.float32, device=dev)
+    am8 = torch.empty((8,), dtype=torch.int32, device=dev)
+    us = graph_time(lambda: w4.w4a16_gemv_argmax(x8, q, sc, out=y8, argmax=am8, stream=stream), reps=10)
+    b = stage_bytes(N, K, 8) + 4 * 8
+    res["vocab_argmax_262144x1536_m8"] = {"us": us, "GBps": b / us / 1e3, "bytes": b}
+    del x8, y8, am8
 
     if sweep is not None:
         # One token's weight reads: the 140-call sweep then the vocabulary

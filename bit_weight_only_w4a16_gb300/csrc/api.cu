@@ -190,6 +190,12 @@ int w4a16_gemv(float *y, const uint16_t *x, const uint32_t *qweight, const uint1
             cudaError_t e = w4::run_decode_m1(mp, y, x, qweight, scales, N, K, lg, s);
             return e == cudaSuccess ? W4_OK : cuda_fail(e);
         }
+    } else {
+        const w4::Slots8Plan sp = w4::plan_slots8(M, N, K, st->num_sms, lg, qweight, scales);
+        if (sp.ok) {
+            cudaError_t e = w4::run_decode_slots8(sp, y, x, qweight, scales, M, N, K, nullptr, nullptr, st->err, s);
+            return e == cudaSuccess ? W4_OK : cuda_fail(e);
+        }
     }
     const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
     if (!decode_fits(p, M, K))
@@ -240,6 +246,13 @@ int w4a16_gemv_argmax(float *y, int32_t *argmax, const uint16_t *x, const uint32
         cudaError_t e = w4::run_decode_vocab(y, x, qweight, scales, N, K, lg, st->keys, argmax, st->err,
                                              st->num_sms, s);
         return e == cudaSuccess ? W4_OK : cuda_fail(e);
+    }
+    if (M >= 2) {
+        const w4::Slots8Plan sp = w4::plan_slots8(M, N, K, st->num_sms, lg, qweight, scales);
+        if (sp.ok && (size_t)M * sp.grid <= kKeyCapacity) {
+            cudaError_t e = w4::run_decode_slots8(sp, y, x, qweight, scales, M, N, K, st->keys, argmax, st->err, s);
+            return e == cudaSuccess ? W4_OK : cuda_fail(e);
+        }
     }
     const w4::DecodePlan p = w4::plan_decode(M, N, K, st->num_sms);
     if (!decode_fits(p, M, K) || (size_t)M * p.grid > kKeyCapacity)

@@ -190,6 +190,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t a)
     return v;
 }
 
+__device__ __forceinline__ uint2 lds64(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t a)
 {
     uint32_t v;
@@ -309,6 +316,65 @@ __device__ __forceinline__ void unpack_mma2_f16(float (&c)[4], float (&d)[4], ui
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%4,%5,%6,%7}, {p2,q2,p3,q3}, {%12,%13}, {%4,%5,%6,%7};\n"
         "}\n"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3]), "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(wa), "r"(wb), "r"(x0), "r"(x1), "r"(x2), "r"(x3));
+}
+
+// unpack_mma2 with both mmas chained into one accumulator: c += A(pairs 04,
+// 15) * (x0, x1) + A(pairs 26, 37) * (x2, x3). For the M <= 8 slot form, where
+// lane t holds word t of one 32-code group, so c is that group's partial.
+__device__ __forceinline__ void unpack_mma2_1(float (&c)[4], uint32_t wa, uint32_t wb, uint32_t x0, uint32_t x1,
+                                              uint32_t x2, uint32_t x3)
+{
+    asm("{\n"
+        ".reg .b32 p0, p1, p2, p3, q0, q1, q2, q3, t, m, o, k;\n"
+        "mov.b32 m, 0x000F000F;\n"
+        "mov.b32 o, 0x43004300;\n"
+        "mov.b32 k, 0x43084308;\n"
+        "lop3.b32 p0, %4, m, o, 0xEA;\n"
+        "shr.u32 t, %4, 4;\n lop3.b32 p1, t, m, o, 0xEA;\n"
+        "shr.u32 t, %4, 8;\n lop3.b32 p2, t, m, o, 0xEA;\n"
+        "shr.u32 t, %4, 12;\n lop3.b32 p3, t, m, o, 0xEA;\n"
+        "lop3.b32 q0, %5, m, o, 0xEA;\n"
+        "shr.u32 t, %5, 4;\n lop3.b32 q1, t, m, o, 0xEA;\n"
+        "shr.u32 t, %5, 8;\n lop3.b32 q2, t, m, o, 0xEA;\n"
+        "shr.u32 t, %5, 12;\n lop3.b32 q3, t, m, o, 0xEA;\n"
+        "sub.rn.bf16x2 p0, p0, k;\n sub.rn.bf16x2 p1, p1, k;\n sub.rn.bf16x2 p2, p2, k;\n sub.rn.bf16x2 p3, p3, k;\n"
+        "sub.rn.bf16x2 q0, q0, k;\n sub.rn.bf16x2 q1, q1, k;\n sub.rn.bf16x2 q2, q2, k;\n sub.rn.bf16x2 q3, q3, k;\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {p0,q0,p1,q1}, {%6,%7}, {%0,%1,%2,%3};\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {p2,q2,p3,q3}, {%8,%9}, {%0,%1,%2,%3};\n"
+        "}\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(wa), "r"(wb), "r"(x0), "r"(x1), "r"(x2), "r"(x3));
+}
+
+// The fp16 form of unpack_mma2_1 (x held in fp16; see unpack_mma2_f16).
+__device__ __forceinline__ void unpack_mma2_1_f16(float (&c)[4], uint32_t wa, uint32_t wb, uint32_t x0, uint32_t x1,
+                                                  uint32_t x2, uint32_t x3)
+{
+    asm("{\n"
+        ".reg .b32 p0, p1, p2, p3, q0, q1, q2, q3, t, u, ml, mh, o, k, s, b;\n"
+        "mov.b32 ml, 0x000F000F;\n"
+        "mov.b32 mh, 0x00F000F0;\n"
+        "mov.b32 o, 0x64006400;\n"
+        "mov.b32 k, 0x64086408;\n"
+        "mov.b32 s, 0x2C002C00;\n"
+        "mov.b32 b, 0xD480D480;\n"
+        "lop3.b32 p0, %4, ml, o, 0xEA;\n"
+        "lop3.b32 p1, %4, mh, o, 0xEA;\n"
+        "shr.u32 t, %4, 8;\n"
+        "lop3.b32 p2, t, ml, o, 0xEA;\n"
+        "lop3.b32 p3, t, mh, o, 0xEA;\n"
+        "lop3.b32 q0, %5, ml, o, 0xEA;\n"
+        "lop3.b32 q1, %5, mh, o, 0xEA;\n"
+        "shr.u32 u, %5, 8;\n"
+        "lop3.b32 q2, u, ml, o, 0xEA;\n"
+        "lop3.b32 q3, u, mh, o, 0xEA;\n"
+        "sub.rn.f16x2 p0, p0, k;\n fma.rn.f16x2 p1, p1, s, b;\n sub.rn.f16x2 p2, p2, k;\n fma.rn.f16x2 p3, p3, s, b;\n"
+        "sub.rn.f16x2 q0, q0, k;\n fma.rn.f16x2 q1, q1, s, b;\n sub.rn.f16x2 q2, q2, k;\n fma.rn.f16x2 q3, q3, s, b;\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {p0,q0,p1,q1}, {%6,%7}, {%0,%1,%2,%3};\n"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {p2,q2,p3,q3}, {%8,%9}, {%0,%1,%2,%3};\n"
+        "}\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(wa), "r"(wb), "r"(x0), "r"(x1), "r"(x2), "r"(x3));
 }
 

@@ -484,6 +484,277 @@ w4_decode_slab_kernel(const VocabArgs a, int R, const __grid_constant__ CUtensor
 }
 
 
+// ------------------------------------------------------------ M <= 8 ----
+//
+// The same shared-memory slots for 2..8 x-rows. The mma's eight B columns are
+// the x rows (rows M..7 read a zero region), so each mma must stay inside one
+// 32-code group: lane (g, t) reads word t of a group for its two weight rows
+// with 32-bit shared loads straight out of the swizzled slot (the 8 rows of a
+// load land on 8 different 16-byte granules, so the 32 lanes touch 32 banks),
+// and the two mmas of the group chain into one accumulator that is scaled by
+// the group's steps in fp32. Per 16 x 128 tile this is the M = 1 form's
+// unpack and mma count with 8 code loads in place of 2 and 16 step FMAs.
+// x rows are staged in shared memory permuted into the pair order, chunk c of
+// row m at c ^ (4 (m & 1)) so that the 8 lanes of a 128-bit load phase (rows
+// g, g + 1) hit different banks.
+// Vocabulary sizes: one CTA per SM, warp gw of the grid walks row blocks gw,
+// gw + GW, ..., each as S consecutive six-tile units through its two slots,
+// and stores a row block's outputs (and argmax keys) after its last unit.
+// (Measured on GB300: 262144 x 1536 with the pick 89.6 -> 53.8 us at M = 8,
+// 87.6 -> 52.4 us at M = 4, 56.0 -> 46.9 us at M = 2 against the register
+// forms. The same form with a CTA owning a few row blocks was slower than the
+// register forms on every decode-sweep shape at M = 8: a warp's six-tile unit
+// is too long a serial chain at M = 8 when a CTA holds only a few units.)
+struct Slots8Args {
+    float *y;
+    const uint16_t *x;
+    unsigned long long *keys; // per-(x-row, CTA) argmax keys or null
+    int *err;                 // device error word: bit 0 set when a slot wait ran out
+    int M, N, K;
+};
+
+template <bool ARGMAX>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+w4_decode_slots8_kernel(const Slots8Args a, const __grid_constant__ CUtensorMap codes,
+                        const __grid_constant__ CUtensorMap steps)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) unsigned long long bars[kWarps * kSlots];
+    __shared__ unsigned long long ck[8];
+    unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int W = blockDim.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int nrb = a.N >> 4;
+    const int S = (a.K >> 7) / kTs; // six-tile units per row
+    const int GW = gridDim.x * W, gw = blockIdx.x * W + warp;
+    const int nmine = (nrb > gw ? (nrb - gw + GW - 1) / GW : 0) * S;
+    // Unit f of this warp: row block rb, unit h of the row.
+    auto unit_of = [&](int f, int &rb, int &h) {
+        rb = gw + (f / S) * GW;
+        h = f % S;
+    };
+
+    const uint32_t wslot0 = smem_addr(smem + (size_t)warp * kSlots * kSlotBytes);
+    unsigned char *ssteps = smem + (size_t)W * kSlots * kSlotBytes;
+    const uint32_t wstep0 = smem_addr(ssteps + (size_t)warp * kSlots * kStepBytes);
+    const int cpr = a.K >> 3, nx = a.M * cpr;
+    uint4 *xs = reinterpret_cast<uint4 *>(ssteps + (size_t)W * kSlots * kStepBytes); // [M][cpr]
+    uint4 *zs = xs + nx;                                                               // 16 zero chunks
+
+    const uint32_t bar0 = smem_addr(&bars[warp * kSlots]);
+    const uint64_t policy = policy_evict_first();
+    if (lane == 0) {
+        for (int i = 0; i < kSlots; ++i)
+            mbar_init(bar0 + 8u * i, 1);
+        fence_mbar_init();
+    }
+    if (ARGMAX && threadIdx.x < 8)
+        ck[threadIdx.x] = 0ull;
+    __syncwarp();
+    auto fill = [&](int f) {
+        int rb, h;
+        unit_of(f, rb, h);
+        const uint32_t bar = bar0 + 8u * (f % kSlots);
+        mbar_arrive_expect_tx(bar, (uint32_t)(kSlotBytes + kStepBytes));
+        tma_load_3d(wslot0 + (uint32_t)((f % kSlots) * kSlotBytes), &codes, 0, h * kLines, rb * 16, bar, policy);
+        tma_load_2d(wstep0 + (uint32_t)((f % kSlots) * kStepBytes), &steps, h * kTs * 4, rb * 16, bar, policy);
+    };
+    if (lane == 0)
+        for (int f = 0; f < kSlots && f < nmine; ++f)
+            fill(f);
+    if (threadIdx.x == 32)
+        prefetch_l2_bulk(a.x, (uint32_t)(nx * 16));
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // x rows, permuted and bank-swizzled. When every value is exact in fp16
+    // and a thread holds at most 4 chunks (kept in registers between the check
+    // and the store), the CTA stages fp16 and runs the fp16 unpack.
+    const bool few = nx <= 4 * (int)blockDim.x;
+    bool exact = few;
+    uint4 v[4];
+    if (few) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = threadIdx.x + q * blockDim.x;
+            if (i < nx) {
+                v[q] = permute_x8(*reinterpret_cast<const uint4 *>(a.x + 8 * i));
+                bf16x2_to_f16x2_exact(v[q].x, exact);
+                bf16x2_to_f16x2_exact(v[q].y, exact);
+                bf16x2_to_f16x2_exact(v[q].z, exact);
+                bf16x2_to_f16x2_exact(v[q].w, exact);
+            }
+        }
+    }
+    const bool f16 = __syncthreads_and(exact) != 0;
+    if (few) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = threadIdx.x + q * blockDim.x;
+            if (i < nx) {
+                const int m = i / cpr, c = i - m * cpr;
+                uint4 o = v[q];
+                if (f16) {
+                    bool d = true;
+                    o = make_uint4(bf16x2_to_f16x2_exact(o.x, d), bf16x2_to_f16x2_exact(o.y, d),
+                                   bf16x2_to_f16x2_exact(o.z, d), bf16x2_to_f16x2_exact(o.w, d));
+                }
+                xs[m * cpr + (c ^ (4 * (m & 1)))] = o;
+            }
+        }
+    } else {
+        // Many chunks a thread: all of them in flight at once as asynchronous
+        // 16-byte copies into their swizzled places, then each thread permutes
+        // its own chunks in place (bf16).
+        const uint32_t base = smem_addr(xs);
+        int m = 0, c = threadIdx.x;
+        while (c >= cpr) {
+            c -= cpr;
+            ++m;
+        }
+        const int m_first = m, c_first = c;
+        for (int i = threadIdx.x; i < nx; i += blockDim.x) {
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                             base + 16u * (uint32_t)(m * cpr + (c ^ (4 * (m & 1))))),
+                         "l"(a.x + 8 * (size_t)i)
+                         : "memory");
+            c += blockDim.x;
+            while (c >= cpr) {
+                c -= cpr;
+                ++m;
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        m = m_first;
+        c = c_first;
+        for (int i = threadIdx.x; i < nx; i += blockDim.x) {
+            uint4 *q = xs + m * cpr + (c ^ (4 * (m & 1)));
+            *q = permute_x8(*q);
+            c += blockDim.x;
+            while (c >= cpr) {
+                c -= cpr;
+                ++m;
+            }
+        }
+    }
+    if (threadIdx.x < 16)
+        zs[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+
+    // Lane constants. Weight rows rA, rB = rA + 8 of a row block (mma rows g,
+    // g + 8); x row g (B column g) or the zero region; chunk offsets of group
+    // slot j in a tile; per 128-byte line of row rA its offset and swizzle (row
+    // rB is 24 lines on, with the same swizzle phase).
+    const int rA = perm_row(g);
+    const bool xreal = g < a.M;
+    const uint4 *xb = xreal ? xs + g * cpr : zs;
+    const int xst = xreal ? 16 : 0;
+    const int sw = xreal ? 4 * (g & 1) : 0;
+    int xo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        xo[j] = (4 * j + t) ^ sw;
+    uint32_t coff[kLines], cx[kLines];
+#pragma unroll
+    for (int ll = 0; ll < kLines; ++ll) {
+        const int L = rA * kLines + ll;
+        coff[ll] = (uint32_t)(L * 128 + 4 * t);
+        cx[ll] = (uint32_t)((L & 7) << 4);
+    }
+    const uint32_t stA = (uint32_t)(rA * kTs * 8), stB = stA + 8u * kTs * 8u;
+
+    bool ok = true;
+    int issued = nmine < kSlots ? nmine : kSlots, failed = -1;
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+    auto run = [&](auto f16c) {
+        constexpr bool F16 = decltype(f16c)::value;
+        for (int f = 0; f < nmine; ++f) {
+            const uint32_t bar = bar0 + 8u * (f % kSlots);
+            const uint32_t parity = (uint32_t)((f / kSlots) & 1);
+            if (ok) {
+                const bool done = mbar_wait_bounded(bar, parity, kWaitLimit);
+                ok = __all_sync(0xFFFFFFFFu, done);
+                if (!ok) {
+                    failed = f;
+                    if (lane == 0)
+                        atomicOr(a.err, 1);
+                }
+            }
+            int rb, h;
+            unit_of(f, rb, h);
+            const uint32_t sbase = wslot0 + (uint32_t)((f % kSlots) * kSlotBytes);
+            const uint32_t stbase = wstep0 + (uint32_t)((f % kSlots) * kStepBytes);
+            const uint4 *xh = xb + xst * h * kTs;
+#pragma unroll
+            for (int l = 0; l < kTs; ++l) {
+                const uint2 sa = lds64(stbase + stA + 8u * l), sb = lds64(stbase + stB + 8u * l);
+                const uint32_t cb = sbase + coff[l >> 1];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t ad = cb + (((uint32_t)((4 * (l & 1) + j) << 4)) ^ cx[l >> 1]);
+                    const uint32_t wa = lds32(ad), wb = lds32(ad + 24u * 128u);
+                    const uint4 xv = xh[xst * l + xo[j]];
+                    float c[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (F16)
+                        unpack_mma2_1_f16(c, wa, wb, xv.x, xv.y, xv.z, xv.w);
+                    else
+                        unpack_mma2_1(c, wa, wb, xv.x, xv.y, xv.z, xv.w);
+                    const uint32_t pa = (j >> 1) ? sa.y : sa.x, pb = (j >> 1) ? sb.y : sb.x;
+                    const float s_a = (j & 1) ? bf16hi_to_f32(pa) : bf16lo_to_f32(pa);
+                    const float s_b = (j & 1) ? bf16hi_to_f32(pb) : bf16lo_to_f32(pb);
+                    a0 = fmaf(s_a, c[0], a0);
+                    a1 = fmaf(s_a, c[1], a1);
+                    b0 = fmaf(s_b, c[2], b0);
+                    b1 = fmaf(s_b, c[3], b1);
+                }
+            }
+            // Every lane's reads of this slot are done; lane 0 refills it.
+            __syncwarp();
+            if (ok && f + kSlots < nmine) {
+                if (lane == 0)
+                    fill(f + kSlots);
+                ++issued;
+            }
+            // Lane (g, t) holds x rows 2t, 2t + 1 of weight rows rA, rB.
+            const int m0 = 2 * t, m1 = 2 * t + 1;
+            if (h == S - 1) {
+                const int rowA = rb * 16 + rA, rowB = rowA + 8;
+                if (m0 < a.M) {
+                    a.y[(size_t)m0 * a.N + rowA] = a0;
+                    a.y[(size_t)m0 * a.N + rowB] = b0;
+                    if (ARGMAX) {
+                        atomicMax(&ck[m0], argmax_key(a0, (uint32_t)rowA));
+                        atomicMax(&ck[m0], argmax_key(b0, (uint32_t)rowB));
+                    }
+                }
+                if (m1 < a.M) {
+                    a.y[(size_t)m1 * a.N + rowA] = a1;
+                    a.y[(size_t)m1 * a.N + rowB] = b1;
+                    if (ARGMAX) {
+                        atomicMax(&ck[m1], argmax_key(a1, (uint32_t)rowA));
+                        atomicMax(&ck[m1], argmax_key(b1, (uint32_t)rowB));
+                    }
+                }
+                a0 = a1 = b0 = b1 = 0.f;
+            }
+        }
+    };
+    if (f16)
+        run(std::true_type{});
+    else
+        run(std::false_type{});
+
+    if (failed >= 0 && lane == 0)
+        for (int f = failed; f < issued; ++f)
+            mbar_wait_bounded(bar0 + 8u * (f % kSlots), (uint32_t)((f / kSlots) & 1), kDrainLimit);
+    __syncthreads();
+    if (ARGMAX && threadIdx.x < a.M)
+        a.keys[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = ck[threadIdx.x];
+}
+
 } // namespace
 
 bool vocab_supported(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc)
@@ -650,6 +921,89 @@ cudaError_t run_decode_slab(int R, float *y, const uint16_t *x, const uint32_t *
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, w4_decode_slab_kernel, a, R, map, smap);
+}
+
+// ------------------------------------------------------------ M <= 8 ----
+
+// Shared memory of the M <= 8 slot form with W warps.
+static size_t slots8_smem(int W, int M, int K)
+{
+    return (size_t)W * kSlots * (kSlotBytes + kStepBytes) + (size_t)M * (K / 8) * 16 + 16 * 16 + 1024;
+}
+
+Slots8Plan plan_slots8(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc)
+{
+    Slots8Plan p;
+    if (M < 2 || M > 8 || lg != 0 || K % (kTs * 128) != 0 || N % 16 != 0 || num_sms < 1)
+        return p;
+    if ((reinterpret_cast<uintptr_t>(qw) & 15) != 0 || (reinterpret_cast<uintptr_t>(sc) & 15) != 0 ||
+        tmap_encoder() == nullptr)
+        return p;
+    // As many warps as the shared memory holds; every warp of the wave walks
+    // at least two row blocks.
+    int W = kWarps;
+    while (W >= 4 && slots8_smem(W, M, K) > 226 * 1024)
+        --W;
+    if (W < 4 || N / 16 < 2 * num_sms * W)
+        return p;
+    p.ok = true;
+    p.W = W;
+    p.grid = num_sms;
+    p.smem = slots8_smem(W, M, K);
+    return p;
+}
+
+cudaError_t run_decode_slots8(const Slots8Plan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                              const uint16_t *sc, int M, int N, int K, unsigned long long *keys, int32_t *argmax,
+                              int *err, cudaStream_t s)
+{
+    auto enc = tmap_encoder();
+    if (!enc || !p.ok)
+        return cudaErrorNotSupported;
+    CUtensorMap map, smap;
+    cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)N};
+    cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
+    cuuint32_t box[3] = {32, (cuuint32_t)kLines, 16};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cuuint64_t sd[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
+    cuuint64_t ss[1] = {(cuuint64_t)K / 16};
+    cuuint32_t sbx[2] = {(cuuint32_t)(kTs * 4), 16};
+    cuuint32_t ses[2] = {1, 1};
+    if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(sc), sd, ss, sbx, ses,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    Slots8Args a;
+    a.y = y;
+    a.x = x;
+    a.keys = keys;
+    a.err = err;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    const bool am = argmax != nullptr;
+    auto kern = am ? w4_decode_slots8_kernel<true> : w4_decode_slots8_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(p.W * 32);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, map, smap);
+    if (e != cudaSuccess || !am)
+        return e;
+    return run_argmax_finalize(argmax, keys, M, p.grid, s);
 }
 
 } // namespace w4

@@ -81,6 +81,21 @@ int slab_rows_per_cta(int M, int N, int K, int num_sms, int lg, const void *qw, 
 cudaError_t run_decode_slab(int R, float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int N,
                             int K, int *err, cudaStream_t s);
 
+// Vocabulary-sized decode GEMV for 2..8 x-rows with the same shared-memory
+// slots (group 32, K % 768 == 0, N % 16 == 0, at least two 16-row blocks per
+// warp of a full wave, 16-byte aligned codes and steps, x staged whole in
+// shared memory). With argmax != nullptr the per-(x-row, CTA) keys go to
+// keys[M][grid] and argmax[m] receives the pick of x-row m.
+struct Slots8Plan {
+    bool ok = false;
+    int W = 0, grid = 0;
+    size_t smem = 0;
+};
+Slots8Plan plan_slots8(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc);
+cudaError_t run_decode_slots8(const Slots8Plan &p, float *y, const uint16_t *x, const uint32_t *qw,
+                              const uint16_t *sc, int M, int N, int K, unsigned long long *keys, int32_t *argmax,
+                              int *err, cudaStream_t s);
+
 // argmax[m] = index of the largest key in keys[m][0 .. nblocks), or *forced
 // when forced != nullptr and *forced >= 0.
 cudaError_t run_argmax_finalize(int32_t *argmax, const unsigned long long *keys, int M, int nblocks,

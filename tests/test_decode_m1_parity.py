@@ -86,3 +86,24 @@ def test_m1_deterministic(w4):
         torch.cuda.synchronize()
         for y in ys[1:]:
             assert torch.equal(y.view(torch.int32), ys[0].view(torch.int32)), (N, K)
+
+
+@pytest.mark.parametrize("special", ["none", "large", "tiny", "subnormal", "zeros"])
+@pytest.mark.parametrize("N,K", [(2560, 1536), (24576, 1536), (1536, 6144), (1536, 12288)])
+def test_m1_special_x_values(w4, special, N, K):
+    """The sweep's long M = 1 shapes with x values at the edges of bf16 (2^20,
+    2^-30, a bf16 subnormal) and with runs of exact zeros: the bound against
+    the oracle holds for each."""
+    x, qw, sc = synth.gen_w4_problem(4400 + N % 89 + K % 83, 1, N, K)
+    x = x.copy()
+    if special == "large":
+        x[0, 17] = 0x4980          # 2^20: beyond fp16's range
+    elif special == "tiny":
+        x[0, 300] = 0x3080         # 2^-30: below fp16's subnormal grid
+    elif special == "subnormal":
+        x[0, 5] = 0x0001           # a bf16 subnormal
+    elif special == "zeros":
+        x[0, 64:96] = 0x0000
+    y = _gemv(w4, x, qw, sc, 32)
+    yr, ar = oracle.gemm(x, qw, sc)
+    assert_w4_close(y, yr, ar, what=f"m1 {N}x{K} x {special}")
