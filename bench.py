@@ -786,6 +786,7 @@ def run_ours(args, rank, world):
 def run_ncu_case(case: str):
     """One small fixed case for an ncu capture: no timing, no output but "ok".
 
+    sweep         : the 140 calls of one M=1 decode weight sweep, launched eagerly once.
     decode_shapes : w4a16_gemv, M=1, twice on each of (24576,1536) (1536,12288)
                     (2560,1536) (1536,2048) (1536,6144), writing a 256 MB buffer
                     between calls.
@@ -816,7 +817,16 @@ def run_ncu_case(case: str):
         sc = torch.from_numpy(synth.gen_scales(seed, N, K).view(np.int16)).to(dev)
         return x, q, sc
 
-    if case == "hadamard":
+    if case == "sweep":
+        # The 140 calls of one M=1 decode weight sweep, launched eagerly once (ncu's
+        # launch list of graph-replayed nodes failed to launch the shared-memory
+        # slot kernel; eager launches profile normally).
+        sweep = Sweep(dev, keep_host=False)
+        s = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(s):
+            sweep.run(w4, s)
+        torch.cuda.synchronize()
+    elif case == "hadamard":
         N, K = 262144, 1536
         q = synth.gen_qweight_torch(1000, N, K, dev)
         sc = torch.from_numpy(synth.gen_scales(1000, N, K, 256).view(np.int16)).to(dev)
@@ -914,7 +924,7 @@ def main():
                          "gather, prefill)")
     ap.add_argument("--ncu-case", default=None,
                     help="run one small fixed case for an ncu capture instead of the bench: "
-                         "decode_shapes | m8_shapes | vocab | gather_probe | attn | hadamard | step | prefill:NxK")
+                         "sweep | decode_shapes | m8_shapes | vocab | gather_probe | attn | hadamard | step | prefill:NxK")
     args = ap.parse_args()
     if args.ncu_case:
         run_ncu_case(args.ncu_case)
