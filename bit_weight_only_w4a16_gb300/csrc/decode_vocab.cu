@@ -757,6 +757,36 @@ w4_decode_slots8_kernel(const Slots8Args a, const __grid_constant__ CUtensorMap 
 
 } // namespace
 
+// Tensor maps of the slot kernels: codes as uint32 {32 words, K/256 lines,
+// N rows} with box {32, lines, 16} and the 128-byte swizzle; with steps != null
+// also the group-32 steps as uint16 {K/32, N} with box {steps_box, 16} (its row
+// stride K/16 bytes is a multiple of 16 since K % 256 == 0; the callers check
+// that the base is 16-byte aligned).
+static bool encode_slot_maps(CUtensorMap *codes, CUtensorMap *steps, const uint32_t *qw, const uint16_t *sc, int N,
+                             int K, int lines, int steps_box)
+{
+    auto enc = tmap_encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)N};
+    cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
+    cuuint32_t box[3] = {32, (cuuint32_t)lines, 16};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    if (steps == nullptr)
+        return true;
+    cuuint64_t sd[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
+    cuuint64_t ss[1] = {(cuuint64_t)K / 16};
+    cuuint32_t sbx[2] = {(cuuint32_t)steps_box, 16};
+    cuuint32_t ses[2] = {1, 1};
+    return enc(steps, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(sc), sd, ss, sbx, ses,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool vocab_supported(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc)
 {
     const int nrb = N / 16;
@@ -774,34 +804,14 @@ cudaError_t run_decode_vocab(float *y, const uint16_t *x, const uint32_t *qw, co
                              int lg, unsigned long long *keys, int32_t *argmax, int *err, int num_sms,
                              cudaStream_t s, const int32_t *forced)
 {
-    auto enc = tmap_encoder();
-    if (!enc)
-        return cudaErrorNotSupported;
-    CUtensorMap map;
-    // codes as uint32 {32 words, K/256 chunks, N rows}; box {32, 3, 16}.
-    cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)N};
-    cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
-    cuuint32_t box[3] = {32, (cuuint32_t)kLines, 16};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    // steps (group 32) as uint16 {K/32, N}; box {24, 16}. Its row stride (K/16
-    // bytes) is a multiple of 16 since K % 768 == 0; vocab_supported checked
-    // that the base is 16-byte aligned.
-    CUtensorMap smap = map;
+    // Codes {32, 3, 16} boxes; steps by tensor copy only at group 32 (a steps
+    // row of K/group bf16 is not always a multiple of 16 bytes otherwise).
     const bool g32_tma = lg == 0;
-    if (g32_tma) {
-        cuuint64_t sd[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
-        cuuint64_t ss[1] = {(cuuint64_t)K / 16};
-        cuuint32_t sbx[2] = {(cuuint32_t)(kTs * 4), 16};
-        cuuint32_t ses[2] = {1, 1};
-        if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(sc), sd, ss, sbx, ses,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    CUtensorMap map, smap;
+    if (!encode_slot_maps(&map, g32_tma ? &smap : nullptr, qw, sc, N, K, kLines, kTs * 4))
+        return cudaErrorInvalidValue;
+    if (!g32_tma)
+        smap = map;
     VocabArgs a;
     a.y = y;
     a.x = x;
@@ -872,25 +882,10 @@ int slab_rows_per_cta(int M, int N, int K, int num_sms, int lg, const void *qw, 
 cudaError_t run_decode_slab(int R, float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int N,
                             int K, int *err, cudaStream_t s)
 {
-    auto enc = tmap_encoder();
-    if (!enc || R < 1)
+    if (R < 1)
         return cudaErrorNotSupported;
     CUtensorMap map, smap;
-    cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)N};
-    cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
-    cuuint32_t box[3] = {32, (cuuint32_t)kLines, 16};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    cuuint64_t sd[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
-    cuuint64_t ss[1] = {(cuuint64_t)K / 16};
-    cuuint32_t sbx[2] = {(cuuint32_t)(kTs * 4), 16};
-    cuuint32_t ses[2] = {1, 1};
-    if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(sc), sd, ss, sbx, ses,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (!encode_slot_maps(&map, &smap, qw, sc, N, K, kLines, kTs * 4))
         return cudaErrorInvalidValue;
     VocabArgs a;
     a.y = y;
@@ -957,25 +952,10 @@ cudaError_t run_decode_slots8(const Slots8Plan &p, float *y, const uint16_t *x, 
                               const uint16_t *sc, int M, int N, int K, unsigned long long *keys, int32_t *argmax,
                               int *err, cudaStream_t s)
 {
-    auto enc = tmap_encoder();
-    if (!enc || !p.ok)
+    if (!p.ok)
         return cudaErrorNotSupported;
     CUtensorMap map, smap;
-    cuuint64_t dims[3] = {32, (cuuint64_t)(K / 256), (cuuint64_t)N};
-    cuuint64_t strides[2] = {128, (cuuint64_t)K / 2};
-    cuuint32_t box[3] = {32, (cuuint32_t)kLines, 16};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(qw), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    cuuint64_t sd[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
-    cuuint64_t ss[1] = {(cuuint64_t)K / 16};
-    cuuint32_t sbx[2] = {(cuuint32_t)(kTs * 4), 16};
-    cuuint32_t ses[2] = {1, 1};
-    if (enc(&smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(sc), sd, ss, sbx, ses,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (!encode_slot_maps(&map, &smap, qw, sc, N, K, kLines, kTs * 4))
         return cudaErrorInvalidValue;
     Slots8Args a;
     a.y = y;
