@@ -22,11 +22,13 @@
 //     query held in registers), fp32 accumulation in two chains; the warps'
 //     partial scores (their head-dim slices) are added through shared memory
 //     in warp order, so every warp sees bit-identical scores;
-//   - online softmax in the exp2 domain per head; the weights are rounded to
-//     bf16 for the value product and the running sum adds the rounded weights,
-//     so the normalisation matches the weights actually applied;
-//   - values: mma with the warp's 16 head dims as rows and the 8 heads as
-//     columns (A = value tile transposed by ldmatrix.trans, B = the weights);
+//   - online softmax in the exp2 domain per head; each weight goes to the
+//     value product as two bf16 parts (hi = bf16(p), lo = bf16(p - hi): within
+//     2^-18 of p, against 2^-9 for one bf16) and the running sum adds exactly
+//     those applied weights, so the normalisation matches them;
+//   - values: two mmas (the weights' hi and lo parts) with the warp's 16 head
+//     dims as rows and the 8 heads as columns (A = value tile transposed by
+//     ldmatrix.trans, B = the weights);
 //   - each CTA stores its unnormalised output with its running max and sum; a
 //     second kernel merges the slices in a fixed order (deterministic);
 //   - the query position may live in device memory ("with every position on
@@ -246,8 +248,16 @@ attn_split_kernel(const AttnArgs a)
             for (int j = 0; j < 4; ++j)
                 p[j] = exp2f(sc[j] - m_new); // 0 for masked slots
         }
+        // Each weight as two bf16 parts, hi = bf16(p) and lo = bf16(p - hi) (p - hi
+        // is exact in fp32): the value product applies hi + lo, within 2^-18 of
+        // p, and hi + lo is exact in fp32 (at most 17 significant bits), so the
+        // running sum adds exactly the weights applied.
         const uint32_t pb0 = pack_bf16(p[0], p[1]), pb1 = pack_bf16(p[2], p[3]);
-        float psum = bf16lo_to_f32(pb0) + bf16hi_to_f32(pb0) + bf16lo_to_f32(pb1) + bf16hi_to_f32(pb1);
+        const float h0 = bf16lo_to_f32(pb0), h1 = bf16hi_to_f32(pb0);
+        const float h2 = bf16lo_to_f32(pb1), h3 = bf16hi_to_f32(pb1);
+        const uint32_t pl0 = pack_bf16(p[0] - h0, p[1] - h1), pl1 = pack_bf16(p[2] - h2, p[3] - h3);
+        float psum = (h0 + bf16lo_to_f32(pl0)) + (h1 + bf16hi_to_f32(pl0)) + (h2 + bf16lo_to_f32(pl1)) +
+                     (h3 + bf16hi_to_f32(pl1));
         psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 1);
         psum += __shfl_xor_sync(0xFFFFFFFFu, psum, 2);
         l_run = l_run * alpha + psum;
@@ -269,6 +279,7 @@ attn_split_kernel(const AttnArgs a)
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_t(vb + row * 256 + ((ch ^ (row & 7)) << 4), a0, a1, a2, a3);
                 mma_16816(o[s], a0, a1, a2, a3, pb0, pb1);
+                mma_16816(o[s], a0, a1, a2, a3, pl0, pl1);
             }
         }
     }

@@ -37,3 +37,22 @@ def assert_w4_close(y, y_ref, absy, rel=1e-4, abs_=1e-6, what=""):
                              f"y={y[tuple(i)]!r} ref={y_ref[tuple(i)]!r} err={err[tuple(i)]:.3e} "
                              f"bound={bound[tuple(i)]:.3e}")
     return float((err / np.maximum(absy, 1e-30)).max())
+
+
+def attn_rel_bound(D, S, T):
+    """Relative bound of the decode attention (times sum_t w_t |v_t|), derived
+    from the kernel's arithmetic:
+      2^-16            the value product applies hi + lo of each weight (two bf16
+                       parts, within 2^-18 of the kernel's fp32 weight) and the
+                       normaliser adds those applied weights: a convex combination
+                       with weights within 2 * 2^-18 relative, doubled for margin;
+      2^-19            exp2f (2 ulp) and the roundings of its argument;
+      2 D 2^-23 S      the fp32 score sums over D products (S = max over kept
+                       slots of scale * sum_d |q_d k_d|; a score error e moves a
+                       weight by at most a factor e^(2e));
+      (2 T/16 + 64) 2^-23  the fp32 accumulation of the outputs and the normaliser
+                       along the longest chain: a rescale and an add per 16-token
+                       tile (all tiles in one slice at worst), the mma's own sums
+                       and the merge of the slices."""
+    import math
+    return 2.0 ** -16 + 2.0 ** -19 + 2.0 * D * 2.0 ** -23 * S + (2 * math.ceil(T / 16) + 64) * 2.0 ** -23

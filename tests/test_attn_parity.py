@@ -1,13 +1,11 @@
 """GPU parity of w4_attn_decode against the fp64 oracle (through the C ABI).
 
 Tolerance (derived from the kernel's arithmetic, elementwise):
-  |out - ref| <= (2^-8 + 2 * D * 2^-23 * S) * sum_t w_t |v_t| + 1e-6
+  |out - ref| <= attn_rel_bound(D, S, T) * sum_t w_t |v_t| + 1e-6
 where w are the exact softmax weights (the oracle's absout is sum_t w_t |v_t|)
-and S = max over kept slots of scale * sum_d |q_d k_d|. The first term is the
-bf16 rounding of the weights (relative 2^-9 each; the normalising sum adds the
-rounded weights, so the output is a convex combination with weights within
-2 * 2^-9 of the exact ones); the second bounds the fp32 accumulation of the
-scores (a score error e changes a weight by at most a factor e^(2e)).
+and S = max over kept slots of scale * sum_d |q_d k_d|; the terms are given in
+_util.attn_rel_bound (weights applied as two bf16 parts, exp2, the fp32 score
+sums, the fp32 accumulation chain).
 """
 import numpy as np
 import pytest
@@ -15,7 +13,7 @@ import pytest
 import oracle
 import synth
 
-from _util import to_dev_bits16
+from _util import attn_rel_bound, to_dev_bits16
 from _guard import guarded
 
 pytestmark = pytest.mark.gpu
@@ -51,7 +49,7 @@ def _check(q, k, v, kpos, qpos, window, scale, what):
     got = out.cpu().numpy().astype(np.float64)
     ref, absout = oracle.attn_decode(q, k, v, kpos, qpos=qpos, window=window, scale=scale)
     S = _score_scale(q, k, _keep(kpos, T, qpos, window), scale)
-    rel = 2.0 ** -8 + 2.0 * D * 2.0 ** -23 * S
+    rel = attn_rel_bound(D, S, T)
     err = np.abs(got - ref)
     bound = rel * absout + 1e-6
     bad = err > bound

@@ -21,7 +21,7 @@ import pytest
 
 import oracle
 import synth
-from _util import assert_w4_close, bits16, to_dev_bits16, to_dev_u32
+from _util import assert_w4_close, attn_rel_bound, bits16, to_dev_bits16, to_dev_u32
 from _guard import check_all, gempty, gfrom, gfull, guarded, gzeros
 
 pytestmark = pytest.mark.gpu
@@ -52,7 +52,7 @@ def _attn_close(got, q, k, v, kpos, qpos, window, scale, what):
         kf = np.abs(synth.bf16_bits_to_f32(k[keep]).astype(np.float64))
         S = float(scale * (qf @ kf.T).max())
     D = q.shape[1]
-    bound = (2.0 ** -8 + 2.0 * D * 2.0 ** -23 * S) * absout + 1e-6
+    bound = attn_rel_bound(D, S, T) * absout + 1e-6
     err = np.abs(np.asarray(got, np.float64) - ref)
     assert (err <= bound).all(), f"{what}: worst ratio {(err / bound).max():.3f}"
 
