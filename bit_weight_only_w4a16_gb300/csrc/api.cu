@@ -352,10 +352,18 @@ int w4a16_gemv_hadamard(float *y, int32_t *argmax, const uint16_t *x, const uint
     if ((rc = device_state(&st)) != W4_OK)
         return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // One x-row, blocks of 256 or 512, K % 128 == 0, the M <= 2 kernel (not
-    // its large-N form, where the separate transform overlaps the weight
-    // preload and measured faster): the decode kernel forms x H itself while
-    // staging x (no transform launch, no scratch rows).
+    // One x-row, blocks of 256 or 512, K % 128 == 0, the shared-memory slot
+    // form or the M <= 2 kernel (not the large-N forms, where the separate
+    // transform overlaps the weight preload and measured faster): the decode
+    // kernel forms x H itself while staging x (no transform launch, no scratch
+    // rows).
+    if (M == 1 && !argmax) {
+        const int R = w4::slab_rows_per_cta(M, N, K, st->num_sms, w4::group_shift(group), qweight, scales, hblock);
+        if (R > 0) {
+            cudaError_t e = w4::run_decode_slab(R, y, x, qweight, scales, N, K, st->err, s, hblock);
+            return e == cudaSuccess ? W4_OK : cuda_fail(e);
+        }
+    }
     if (M == 1 && (hblock == 256 || hblock == 512) && K % 128 == 0) {
         const w4::DecodePlan p = w4::plan_decode(2, N, K, st->num_sms);
         if (p.kernel == 2 && decode_fits(p, 2, K) && (!argmax || (size_t)p.grid <= kKeyCapacity)) {

@@ -410,6 +410,86 @@ __device__ __forceinline__ uint32_t bf16x2_of_codes(uint32_t w, int shift, float
     return *reinterpret_cast<uint32_t *>(&r);
 }
 
+// Fused rotation for the Hadamard-rotated GEMV at M = 1 (blocks of b = 32 * PL
+// values, PL = 8 or 16, K % 128 == 0; used by the M <= 2 register-preload
+// kernel and the shared-memory slot form below vocabulary sizes): xs[0 .. cpr)
+// and xs[cpr .. 2 cpr) become the rows hi = bf16(v), lo = bf16(v - hi) of v =
+// (x H)[k] (times norm), each 8-value chunk permuted as permute_x8 lays it out.
+// Warp w transforms blocks w, w + nwarps, ...: lane l holds values
+// [PL*l, PL*l + PL) of the block in registers, so the butterfly stages over
+// the low log2(PL) index bits stay in the lane and the next 5 are lane-bit
+// exchanges (shfl_xor). Stage order and pairing (p + q, p - q) are those of
+// the standalone transform kernel, so both paths give the same bits. All of a
+// warp's x loads are issued before its first stage.
+template <int PL>
+__device__ __forceinline__ void stage_x_hadamard(uint4 *xs, const uint16_t *x, int K, int cpr, float norm)
+{
+    constexpr int B = 32 * PL, NC = PL / 8; // values and 8-value chunks per lane
+    constexpr int kMaxBlk = 1;             // blocks a warp keeps in flight
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int blk0 = threadIdx.x >> 5; blk0 * B < K; blk0 += kMaxBlk * nw) {
+        uint4 raw[kMaxBlk][NC];
+#pragma unroll
+        for (int q = 0; q < kMaxBlk; ++q) {
+            const int blk = blk0 + q * nw;
+#pragma unroll
+            for (int c = 0; c < NC; ++c)
+                raw[q][c] = blk * B < K ? *reinterpret_cast<const uint4 *>(x + blk * B + lane * PL + 8 * c)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < kMaxBlk; ++q) {
+            const int blk = blk0 + q * nw;
+            if (blk * B >= K)
+                break;
+            float v[PL];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                const uint32_t u[4] = {raw[q][c].x, raw[q][c].y, raw[q][c].z, raw[q][c].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[8 * c + 2 * j] = bf16lo_to_f32(u[j]);
+                    v[8 * c + 2 * j + 1] = bf16hi_to_f32(u[j]);
+                }
+            }
+#pragma unroll
+            for (int h = 1; h < PL; h <<= 1)
+#pragma unroll
+                for (int r = 0; r < PL; ++r)
+                    if (!(r & h)) {
+                        const float pv = v[r], qv = v[r + h];
+                        v[r] = pv + qv;
+                        v[r + h] = pv - qv;
+                    }
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int r = 0; r < PL; ++r) {
+                    const float o = __shfl_xor_sync(0xFFFFFFFFu, v[r], m);
+                    v[r] = upper ? o - v[r] : v[r] + o;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float r0 = v[8 * c + 2 * j] * norm, r1 = v[8 * c + 2 * j + 1] * norm;
+                    const __nv_bfloat16 h0 = __float2bfloat16_rn(r0), h1 = __float2bfloat16_rn(r1);
+                    const __nv_bfloat16 l0 = __float2bfloat16_rn(r0 - __bfloat162float(h0));
+                    const __nv_bfloat16 l1 = __float2bfloat16_rn(r1 - __bfloat162float(h1));
+                    hw[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+                    lw[j] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+                }
+                const int cc = ((blk * B + lane * PL) >> 3) + c;
+                xs[cc] = permute_x8(make_uint4(hw[0], hw[1], hw[2], hw[3]));
+                xs[cpr + cc] = permute_x8(make_uint4(lw[0], lw[1], lw[2], lw[3]));
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------- argmax ----
 
 // Order-preserving 64-bit key of (value, index): a larger value wins, and for

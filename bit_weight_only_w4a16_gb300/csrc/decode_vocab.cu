@@ -345,10 +345,17 @@ constexpr size_t kSmem = (size_t)kWarps * kSlots * kSlotBytes; // + steps (group
 // staged, each warp computes its units from shared memory and leaves each
 // unit's 16 row partials in shared memory; the partials of a row are added in
 // slice order (deterministic). Group 32 only (steps by tensor copy).
+// PL = 8 or 16 (Hadamard-rotated weights, blocks of 32 PL): the CTA forms the
+// (hi, lo) rows of x H while staging x (norm = 1/sqrt(block)); B column s
+// carries hi restricted to group slot s and column 4 + s the lo row, so lanes
+// t and t + 2 hold the two rows' partials of the same groups, added with the
+// slot pair.
+template <int PL>
 __global__ void __launch_bounds__(kWarps * 32, 1)
-w4_decode_slab_kernel(const VocabArgs a, int R, const __grid_constant__ CUtensorMap codes,
+w4_decode_slab_kernel(const VocabArgs a, int R, float norm, const __grid_constant__ CUtensorMap codes,
                       const __grid_constant__ CUtensorMap steps)
 {
+    constexpr bool ROT = PL > 0;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) unsigned long long bars[kWarps * kSlots];
     unsigned char *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -366,9 +373,9 @@ w4_decode_slab_kernel(const VocabArgs a, int R, const __grid_constant__ CUtensor
     const uint32_t wslot0 = smem_addr(smem + (size_t)warp * kSlots * kSlotBytes);
     unsigned char *ssteps = smem + (size_t)W * kSlots * kSlotBytes;
     const uint32_t wstep0 = smem_addr(ssteps + (size_t)warp * kSlots * kStepBytes);
-    uint4 *xs = reinterpret_cast<uint4 *>(ssteps + (size_t)W * kSlots * kStepBytes);
+    uint4 *xs = reinterpret_cast<uint4 *>(ssteps + (size_t)W * kSlots * kStepBytes); // [ROT ? 2 : 1][nchunk]
     const int nchunk = a.K >> 3;
-    uint4 *zs = xs + nchunk + 2;
+    uint4 *zs = xs + (ROT ? 2 : 1) * nchunk + 2;
     float *red = reinterpret_cast<float *>(zs + 6); // [nunits][16]
 
     const uint32_t bar0 = smem_addr(&bars[warp * kSlots]);
@@ -397,15 +404,21 @@ w4_decode_slab_kernel(const VocabArgs a, int R, const __grid_constant__ CUtensor
     pdl_launch_dependents();
     pdl_wait();
 
-    for (int i = threadIdx.x; i < nchunk; i += blockDim.x)
-        xs[i] = permute_x8(*reinterpret_cast<const uint4 *>(a.x + 8 * i));
+    if (ROT)
+        stage_x_hadamard<(ROT ? PL : 8)>(xs, a.x, a.K, nchunk, norm);
+    else
+        for (int i = threadIdx.x; i < nchunk; i += blockDim.x)
+            xs[i] = permute_x8(*reinterpret_cast<const uint4 *>(a.x + 8 * i));
     if (threadIdx.x < 4)
         zs[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
 
+    // Lane (g, t) feeds B column g: x (the hi row) restricted to group slot t
+    // when g == t, the lo row when g == t + 4 (rotated), else the zero region.
     const bool bsel = g < 4 && t == g;
-    const uint4 *xlane = bsel ? xs + 4 * t : zs;
-    const int xstep = bsel ? 16 : 0;
+    const bool blo = ROT && g >= 4 && t == g - 4;
+    const uint4 *xlane = bsel ? xs + 4 * t : (blo ? xs + nchunk + 4 * t : zs);
+    const int xstep = (bsel || blo) ? 16 : 0;
     const int rA = perm_row(g), rB = rA + 8;
     const int jt = 2 * (t & 1);
 
@@ -459,9 +472,14 @@ w4_decode_slab_kernel(const VocabArgs a, int R, const __grid_constant__ CUtensor
                 fill(f + kSlots);
             ++issued;
         }
-        // Lanes t, t ^ 1 hold group slots (0, 1) and (2, 3) of the unit's rows.
-        const float vA = accA + __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
-        const float vB = accB + __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+        // Lanes t, t ^ 1 hold group slots (0, 1) and (2, 3) of the unit's rows
+        // (rotated: lanes t + 2 the lo row's).
+        float vA = accA + __shfl_xor_sync(0xFFFFFFFFu, accA, 1);
+        float vB = accB + __shfl_xor_sync(0xFFFFFFFFu, accB, 1);
+        if (ROT) {
+            vA += __shfl_xor_sync(0xFFFFFFFFu, vA, 2);
+            vB += __shfl_xor_sync(0xFFFFFFFFu, vB, 2);
+        }
         if (t == 0) {
             red[u * 16 + rA] = vA;
             red[u * 16 + rB] = vB;
@@ -845,18 +863,19 @@ cudaError_t run_decode_vocab(float *y, const uint16_t *x, const uint32_t *qw, co
     return run_argmax_finalize(argmax, keys, 1, num_sms, s, a.forced);
 }
 
-// Shared memory of the slab form for W warps, and the warp count it launches
-// with: 16 when that fits (and the units fill the slots), else 8; 0 if neither
-// holds every unit within the slots.
-static size_t slab_smem(int W, int R, int S, int K)
+// Shared memory of the slab form for W warps (x rows: 2 when rotated), and the
+// warp count it launches with: 16 when that fits (and the units fill the
+// slots), else 8; 0 if neither holds every unit within the slots.
+static size_t slab_smem(int W, int R, int S, int K, bool rot)
 {
-    return (size_t)W * kSlots * (kSlotBytes + kStepBytes) + (size_t)(K / 8 + 8) * 16 + (size_t)R * S * 16 * 4 + 1024;
+    return (size_t)W * kSlots * (kSlotBytes + kStepBytes) + (size_t)((rot ? 2 : 1) * (K / 8) + 8) * 16 +
+           (size_t)R * S * 16 * 4 + 1024;
 }
 
-static int slab_warps(int R, int S, int K)
+static int slab_warps(int R, int S, int K, bool rot)
 {
     for (int W = kWarps; W >= 8; W /= 2)
-        if (R * S <= W * kSlots && slab_smem(W, R, S, K) <= 226 * 1024)
+        if (R * S <= W * kSlots && slab_smem(W, R, S, K, rot) <= 226 * 1024)
             return W;
     return 0;
 }
@@ -864,23 +883,25 @@ static int slab_warps(int R, int S, int K)
 // Row blocks per CTA of the slab form and whether it serves (N, K): group 32,
 // K % 768 == 0, N % 16 == 0, 16-byte aligned codes and steps, a CTA's units
 // within its 32 slots (so every copy is issued before the dependency wait),
-// below vocabulary sizes.
-int slab_rows_per_cta(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc)
+// below vocabulary sizes; hblock (256 or 512): rotated weights.
+int slab_rows_per_cta(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc, int hblock)
 {
     if (M != 1 || lg != 0 || K % (kTs * 128) != 0 || N % 16 != 0 || num_sms < 1)
+        return 0;
+    if (hblock != 0 && ((hblock != 256 && hblock != 512) || K % hblock != 0))
         return 0;
     if ((reinterpret_cast<uintptr_t>(qw) & 15) != 0 || (reinterpret_cast<uintptr_t>(sc) & 15) != 0 ||
         tmap_encoder() == nullptr)
         return 0;
     const int nrb = N / 16, S = K / (kTs * 128);
     const int R = (nrb + num_sms - 1) / num_sms;
-    if (nrb >= 2 * num_sms * kWarps || slab_warps(R, S, K) == 0)
+    if (nrb >= 2 * num_sms * kWarps || slab_warps(R, S, K, hblock != 0) == 0)
         return 0;
     return R;
 }
 
 cudaError_t run_decode_slab(int R, float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int N,
-                            int K, int *err, cudaStream_t s)
+                            int K, int *err, cudaStream_t s, int hblock)
 {
     if (R < 1)
         return cudaErrorNotSupported;
@@ -897,12 +918,15 @@ cudaError_t run_decode_slab(int R, float *y, const uint16_t *x, const uint32_t *
     a.N = N;
     a.K = K;
     a.lg = 0;
+    const bool rot = hblock != 0;
     const int S = K / (kTs * 128), nrb = N / 16;
-    const int W = slab_warps(R, S, K);
+    const int W = slab_warps(R, S, K, rot);
     if (W == 0)
         return cudaErrorNotSupported;
-    const size_t smem = slab_smem(W, R, S, K);
-    cudaError_t e = cudaFuncSetAttribute(w4_decode_slab_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem = slab_smem(W, R, S, K, rot);
+    auto kern = !rot ? w4_decode_slab_kernel<0>
+                     : (hblock == 256 ? w4_decode_slab_kernel<8> : w4_decode_slab_kernel<16>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -915,7 +939,8 @@ cudaError_t run_decode_slab(int R, float *y, const uint16_t *x, const uint32_t *
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, w4_decode_slab_kernel, a, R, map, smap);
+    const float norm = rot ? 1.0f / sqrtf((float)hblock) : 0.f;
+    return cudaLaunchKernelEx(&cfg, kern, a, R, norm, map, smap);
 }
 
 // ------------------------------------------------------------ M <= 8 ----

@@ -77,9 +77,11 @@ cudaError_t run_decode_vocab(float *y, const uint16_t *x, const uint32_t *qw, co
 // The decode sweep's long M = 1 projections with the same shared-memory slots:
 // rows per CTA when the form serves (N, K) (group 32, K % 768 == 0, N % 16 == 0,
 // 16-byte aligned codes and steps, a CTA's slices within its slots), else 0.
-int slab_rows_per_cta(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc);
+// hblock (256 or 512; 0 for plain weights): Hadamard-rotated weights, the
+// kernel forms the (hi, lo) rows of x H (blocks of hblock) while staging x.
+int slab_rows_per_cta(int M, int N, int K, int num_sms, int lg, const void *qw, const void *sc, int hblock = 0);
 cudaError_t run_decode_slab(int R, float *y, const uint16_t *x, const uint32_t *qw, const uint16_t *sc, int N,
-                            int K, int *err, cudaStream_t s);
+                            int K, int *err, cudaStream_t s, int hblock = 0);
 
 // Vocabulary-sized decode GEMV for 2..8 x-rows with the same shared-memory
 // slots (group 32, K % 768 == 0, N % 16 == 0, at least two 16-row blocks per

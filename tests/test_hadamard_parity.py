@@ -37,7 +37,12 @@ def w4():
                                            # fused into the decode kernel's staging (M = 1, blocks of
                                            # 256 / 512): many blocks per warp, one block, ragged N
                                            (1, 1536, 12288, 512, 256), (1, 48, 256, 256, 32),
-                                           (1, 4000, 2048, 256, 64)])
+                                           (1, 4000, 2048, 256, 64),
+                                           # the shared-memory slot form (group 32, K % 768 == 0):
+                                           # the rotated sweep's long shapes, a shorter last CTA
+                                           (1, 24576, 1536, 512, 32), (1, 1536, 12288, 512, 32),
+                                           (1, 12288, 1536, 256, 32), (1, 1536, 6144, 512, 32),
+                                           (1, 2576, 1536, 256, 32)])
 def test_rotated_gemv_matches_oracle(w4, M, N, K, b, group):
     import torch
     x = synth.gen_x(900 + M + b, M, K)
