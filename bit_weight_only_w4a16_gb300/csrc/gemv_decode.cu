@@ -37,6 +37,9 @@
 #include "common.cuh"
 #include "internal.h"
 
+#include <atomic>
+#include <mutex>
+
 namespace w4 {
 
 static constexpr int kTileK = 128; // k per tile of the m2 kernel: 4 groups
@@ -730,25 +733,37 @@ w4_decode_m8_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 }
 
 // U = 8 (8 quads in flight, ~160 registers) runs CTAs of at most 12 warps.
-template <int U, bool ARGMAX, bool PAIRS>
+// CL4 (no pick, no pairs; a launch with clusters of 4 CTAs): the 4 CTAs of a
+// cluster share 4 row blocks, CTA r takes K quarter r of all four (ksplit is
+// the split within the CTA), so each CTA stages only its quarter of x; each
+// CTA's sums go to the row block's owner (rank = row block within the
+// cluster) through distributed shared memory and are added there in rank
+// order. At M = 8 the bytes an SM takes in set the x staging time (x is
+// 8 K bf16 per CTA: 196 KB at K = 12288).
+template <int U, bool ARGMAX, bool PAIRS, bool CL4>
 __global__ void __launch_bounds__(U == 8 ? 384 : 512)
 w4_decode_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
                const uint32_t *__restrict__ qw, const uint16_t *__restrict__ sc,
                int M, int N, int K, int ksplit, unsigned long long *__restrict__ keys, int lg)
 {
     extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ float recv[CL4 ? 4 * 8 * 16 : 1]; // [sender rank][x-row][row] (CL4)
+    if (CL4) // every CTA of the cluster has started before any remote store
+        asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int nwarps = blockDim.x >> 5;
     const int rbc = nwarps / ksplit;
     const int ks = warp % ksplit, rbl = warp / ksplit;
+    const int crank = CL4 ? (int)cluster_rank() : 0;
     const int nrb = (N + 15) >> 4;
-    const int rb = blockIdx.x * rbc + rbl;
+    const int rb = (CL4 ? (int)(blockIdx.x >> 2) * 4 : (int)blockIdx.x * rbc) + rbl;
     const bool active = rb < nrb;
     const int ngroups = K >> 5;
     const int nquads = ngroups >> 2; // 4-group (128-k) units, K % 128 == 0
-    const int Q0 = (int)((long long)nquads * ks / ksplit);
-    const int nQ = (int)((long long)nquads * (ks + 1) / ksplit) - Q0;
+    const int kst = CL4 ? 4 * ksplit : ksplit, ksi = CL4 ? crank * ksplit + ks : ks;
+    const int Q0 = (int)((long long)nquads * ksi / kst);
+    const int nQ = (int)((long long)nquads * (ksi + 1) / kst) - Q0;
 
     const int rowA = rb * 16 + g, rowB = rowA + 8;
     const int rA = min(rowA, N - 1), rB = min(rowB, N - 1);
@@ -792,7 +807,27 @@ w4_decode_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
 
     uint4 *xs = reinterpret_cast<uint4 *>(smem); // [8][K/8] permuted chunks
     const int cpr = K >> 3;
-    stage_x_rows_async(xs, x, M, K);
+    if (CL4) {
+        // This CTA's K quarter of each x row (the chunks of its quads), all
+        // copies in flight at once, then permuted in place by their owners.
+        const int c0 = 16 * (int)((long long)nquads * crank / 4);
+        const int nc = 16 * (int)((long long)nquads * (crank + 1) / 4) - c0;
+        const uint32_t base = smem_addr(xs);
+        for (int i = threadIdx.x; i < M * nc; i += blockDim.x) {
+            const int m = i / nc, c = c0 + (i - m * nc);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(base + 16u * (uint32_t)(m * cpr + c)),
+                         "l"(x + (size_t)m * K + 8 * c)
+                         : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        for (int i = threadIdx.x; i < M * nc; i += blockDim.x) {
+            const int m = i / nc, c = c0 + (i - m * nc);
+            xs[m * cpr + c] = permute_x8(xs[m * cpr + c]);
+        }
+    } else {
+        stage_x_rows_async(xs, x, M, K);
+    }
     if (M < 8) // rows M..7 of the B operand are zero
         for (int i = M * cpr + threadIdx.x; i < 8 * cpr; i += blockDim.x)
             xs[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -838,6 +873,37 @@ w4_decode_m8q_kernel(float *__restrict__ y, const uint16_t *__restrict__ x,
         }
     }
 
+    if (CL4) {
+        // Sums of this CTA's K quarter per (row block, x-row, row), in warp
+        // order, stored into the owning CTA's recv[crank]; after the cluster
+        // barrier each owner adds the four quarters in rank order.
+        float *red = reinterpret_cast<float *>(xs + 8 * cpr); // [rbc][ksplit][8][16]
+        red[((rbl * ksplit + ks) * 8 + 2 * t) * 16 + g] = a0;
+        red[((rbl * ksplit + ks) * 8 + 2 * t) * 16 + g + 8] = b0;
+        red[((rbl * ksplit + ks) * 8 + 2 * t + 1) * 16 + g] = a1;
+        red[((rbl * ksplit + ks) * 8 + 2 * t + 1) * 16 + g + 8] = b1;
+        __syncthreads();
+        asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+        const uint32_t rbase = smem_addr(recv);
+        for (int i = threadIdx.x; i < rbc * 8 * 16; i += blockDim.x) {
+            const int rr = i & 15, mm = (i >> 4) & 7, rl = i >> 7;
+            float sum = 0.f;
+            for (int k2 = 0; k2 < ksplit; ++k2)
+                sum += red[((rl * ksplit + k2) * 8 + mm) * 16 + rr];
+            const uint32_t dst = map_rank(rbase + 4u * (uint32_t)((crank * 8 + mm) * 16 + rr), (uint32_t)rl);
+            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(dst), "f"(sum) : "memory");
+        }
+        cluster_sync();
+        const int row0 = ((int)(blockIdx.x >> 2) * 4 + crank) * 16;
+        for (int i = threadIdx.x; i < 8 * 16; i += blockDim.x) {
+            const int rr = i & 15, mm = i >> 4;
+            if (mm < M && row0 + rr < N)
+                y[(size_t)mm * N + row0 + rr] =
+                    ((recv[(0 * 8 + mm) * 16 + rr] + recv[(1 * 8 + mm) * 16 + rr]) + recv[(2 * 8 + mm) * 16 + rr]) +
+                    recv[(3 * 8 + mm) * 16 + rr];
+        }
+        return;
+    }
     m8_store<ARGMAX, PAIRS>(y, a0, a1, b0, b1, M, N, g, t, rowA, rowB, active, ksplit, ks, rbl, rbc,
                             reinterpret_cast<float *>(xs + 8 * cpr), keys);
 }
@@ -1064,6 +1130,42 @@ static cudaError_t set_smem(Kern kern, size_t bytes)
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// Clusters of 4 CTAs of the M <= 8 quad kernel's cluster form (16 warps,
+// shared memory for x at K = 12288) that can be resident at once on the
+// current device (clusters must sit in one GPC), cached per device; 0 if the
+// query fails.
+static int m8_cluster_capacity()
+{
+    static std::atomic<int> cap[64];
+    static std::once_flag once[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;
+    std::call_once(once[dev], [dev] {
+        int n = 0;
+        const size_t smem = (size_t)8 * 12288 * 2 + (size_t)4 * 4 * 8 * 16 * sizeof(float);
+        auto ck = w4_decode_m8q_kernel<4, false, false, true>;
+        if (cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(4);
+            cfg.blockDim = dim3(512);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 4;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, ck, &cfg) != cudaSuccess)
+                n = 0;
+        }
+        cudaGetLastError();
+        cap[dev].store(n);
+    });
+    return cap[dev].load();
+}
+
 DecodePlan plan_decode(int M, int N, int K, int num_sms)
 {
     DecodePlan p;
@@ -1188,6 +1290,16 @@ DecodePlan plan_decode(int M, int N, int K, int num_sms)
                 break;
             p = q;
         }
+        // Long K, one row block per CTA with K over 16 warps (the 1536-row down
+        // projections): clusters of 4 CTAs sharing 4 row blocks, each CTA a K
+        // quarter of all four (4 warps per row block), so each stages a
+        // quarter of x.
+        if (p.kernel == 8 && p.ksplit == 16 && p.warps == 16 && K % kTileK == 0 && K >= 4096 && nrb % 4 == 0 &&
+            nrb <= num_sms && m8_cluster_capacity() * 4 >= nrb) {
+            p.cluster = 4;
+            p.ksplit = 4;
+            p.grid = nrb;
+        }
         return p;
     }
     const int rbc = p.warps / p.ksplit;
@@ -1242,8 +1354,32 @@ static cudaError_t launch_m8(const DecodePlan &p, float *y, const uint16_t *x, c
     auto kern = w4_decode_m8_kernel<8, ARGMAX, PAIRS>;
     // 128-bit code loads with a quad transpose when K % 128 == 0 and the steps
     // allow 8-byte loads.
-    if (K % kTileK == 0 && (reinterpret_cast<uintptr_t>(sc) & 7) == 0)
-        kern = p.unroll == 8 ? w4_decode_m8q_kernel<8, ARGMAX, PAIRS> : w4_decode_m8q_kernel<4, ARGMAX, PAIRS>;
+    if (K % kTileK == 0 && (reinterpret_cast<uintptr_t>(sc) & 7) == 0) {
+        kern = p.unroll == 8 ? w4_decode_m8q_kernel<8, ARGMAX, PAIRS, false>
+                             : w4_decode_m8q_kernel<4, ARGMAX, PAIRS, false>;
+        if (!ARGMAX && !PAIRS && p.cluster == 4) {
+            auto ck = p.unroll == 8 ? w4_decode_m8q_kernel<8, false, false, true>
+                                    : w4_decode_m8q_kernel<4, false, false, true>;
+            cudaError_t e = set_smem(ck, smem);
+            if (e != cudaSuccess)
+                return e;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(p.grid);
+            cfg.blockDim = dim3(32 * p.warps);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = s;
+            cudaLaunchAttribute attr[2];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            attr[1].id = cudaLaunchAttributeClusterDimension;
+            attr[1].val.clusterDim.x = 4;
+            attr[1].val.clusterDim.y = 1;
+            attr[1].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 2;
+            return cudaLaunchKernelEx(&cfg, ck, y, x, qw, sc, M, N, K, p.ksplit, keys, lg);
+        }
+    }
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;

@@ -26,6 +26,7 @@ struct DecodePlan {
     int warps = 8;  // warps per CTA
     int unroll = 4; // k-tiles (m2) or groups (m8) in flight per warp
     int grid = 1;
+    int cluster = 1; // 4: the M <= 8 kernel's K quarters over clusters of 4 CTAs (ksplit is per CTA)
 };
 
 DecodePlan plan_decode(int M, int N, int K, int num_sms);

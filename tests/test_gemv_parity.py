@@ -298,3 +298,21 @@ def test_large_n_m8_steps_only_4_byte_aligned(w4):
     rows = np.array([0, 1, 40000, N - 1])
     yr, ar = oracle.gemm(x, synth.gen_qweight_rows(seed, N, K, rows), sc[rows])
     assert_w4_close(y4.cpu().numpy()[:, rows], yr, ar, what="large N M8, 4-byte-aligned steps")
+
+
+@pytest.mark.parametrize("M", [3, 5, 8])
+@pytest.mark.parametrize("N,K", [(1536, 12288), (1536, 6144), (64, 4096), (608, 8192)])
+def test_m8_cluster_k_quarters(w4, M, N, K):
+    """The M <= 8 form whose 1536-row long-K calls run as clusters of 4 CTAs
+    (each CTA a K quarter of 4 row blocks, the quarters added by the owning
+    CTA in rank order): every row against the oracle, all-8 codes exactly zero,
+    and run to run bitwise identical."""
+    import torch
+    x, qw, sc = synth.gen_w4_problem(5600 + M + N % 97 + K % 89, M, N, K)
+    y = _run(w4, x, qw, sc)
+    yr, ar = oracle.gemm(x, qw, sc)
+    assert_w4_close(y, yr, ar, what=f"cluster M{M} N{N} K{K}")
+    y2 = _run(w4, x, qw, sc)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+    z = _run(w4, x, np.full_like(qw, 0x88888888), sc)
+    assert not np.any(z)
