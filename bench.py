@@ -768,7 +768,7 @@ def run_ours(args, rank, world):
                      "traffic_unit": "bytes per sweep (140 launches), ncu dram__bytes_read.sum + "
                                      "dram__bytes_write.sum; null if the kernel changed since",
                      "peak_source": f"{peak_src} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     "kernel": "w4_decode_m1_kernel (q|k|v, o, down F=6144) and w4_decode_m2_kernel (gate|up, down F=12288): all 140 launches of the sweep"},
+                     "kernel": "w4_decode_slab_kernel (q|k|v, gate|up, down) and w4_decode_m1_kernel (o 1536x2048): all 140 launches of the sweep"},
         "probe": {"hbm_read_probe_gbs": probe_gbs, "sweep_frac_of_probe": achieved / probe_gbs},
         "rows": rows,
         "gpu_launches": ncalls * args.steps * len(block_ms),
