@@ -301,12 +301,14 @@ def test_large_n_m8_steps_only_4_byte_aligned(w4):
 
 
 @pytest.mark.parametrize("M", [3, 5, 8])
-@pytest.mark.parametrize("N,K", [(1536, 12288), (1536, 6144), (64, 4096), (608, 8192)])
+@pytest.mark.parametrize("N,K", [(1536, 12288), (1536, 6144), (64, 4096), (608, 8192), (1530, 6144),
+                                 (60, 4096)])
 def test_m8_cluster_k_quarters(w4, M, N, K):
     """The M <= 8 form whose 1536-row long-K calls run as clusters of 4 CTAs
     (each CTA a K quarter of 4 row blocks, the quarters added by the owning
     CTA in rank order): every row against the oracle, all-8 codes exactly zero,
-    and run to run bitwise identical."""
+    and run to run bitwise identical. 1530 and 60 rows end in a ragged row
+    block inside a cluster; 608 rows (38 row blocks) take the one-CTA form."""
     import torch
     x, qw, sc = synth.gen_w4_problem(5600 + M + N % 97 + K % 89, M, N, K)
     y = _run(w4, x, qw, sc)
