@@ -81,6 +81,10 @@ int device_state(DeviceState **out)
             return cuda_fail(e);
         st.ws = static_cast<float *>(w);
         st.num_sms = sms;
+        // One-time lookups that plans use, done here so that a call captured
+        // into a graph later makes none of them.
+        w4::tmap_encoder();
+        w4::m8_cluster_capacity();
         st.ready.store(true, std::memory_order_release);
     }
     *out = &st;

@@ -1134,7 +1134,7 @@ static cudaError_t set_smem(Kern kern, size_t bytes)
 // shared memory for x at K = 12288) that can be resident at once on the
 // current device (clusters must sit in one GPC), cached per device; 0 if the
 // query fails.
-static int m8_cluster_capacity()
+int m8_cluster_capacity()
 {
     static std::atomic<int> cap[64];
     static std::once_flag once[64];

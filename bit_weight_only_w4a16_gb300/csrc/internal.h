@@ -30,6 +30,10 @@ struct DecodePlan {
 };
 
 DecodePlan plan_decode(int M, int N, int K, int num_sms);
+// Clusters of 4 CTAs of the M <= 8 kernel's cluster form that fit on the
+// current device at once (queried once per device, then cached; 0 if the query
+// fails). The device set-up calls it so that no plan queries it under capture.
+int m8_cluster_capacity();
 // Dynamic shared memory the decode kernel of plan p takes for (M, K).
 size_t decode_smem_bytes(const DecodePlan &p, int M, int K);
 
