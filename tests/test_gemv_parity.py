@@ -318,3 +318,40 @@ def test_m8_cluster_k_quarters(w4, M, N, K):
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
     z = _run(w4, x, np.full_like(qw, 0x88888888), sc)
     assert not np.any(z)
+
+
+_CAPTURE_FIRST = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import synth, bit_weight_only_w4a16_gb300 as w4
+from _util import to_dev_bits16, to_dev_u32
+w4.init()
+x, qw, sc = synth.gen_w4_problem(5700, 8, 1536, 12288)
+xd, qd, sd = to_dev_bits16(x), to_dev_u32(qw), to_dev_bits16(sc)
+y = torch.empty((8, 1536), dtype=torch.float32, device="cuda")
+s = torch.cuda.Stream()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):  # the first M = 8 call of the process
+    w4.w4a16_gemm(xd, qd, sd, out=y, stream=s)
+g.replay(); torch.cuda.synchronize()
+ref = w4.w4a16_gemm(xd, qd, sd); torch.cuda.synchronize()
+assert torch.equal(y, ref), "replayed graph differs from the eager call"
+np.save(sys.argv[1], y.cpu().numpy())
+"""
+
+
+def test_m8_cluster_form_captured_as_first_call(w4, tmp_path):
+    """A process whose first M = 8 call (a cluster-form shape) is made under
+    stream capture: the per-device set-up has done the one-time queries, so
+    the capture succeeds, and the replayed graph gives the eager call's bits
+    and the oracle's values."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = tmp_path / "y.npy"
+    code = _CAPTURE_FIRST.format(root=root, tests=os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code, str(out)], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    x, qw, sc = synth.gen_w4_problem(5700, 8, 1536, 12288)
+    yr, ar = oracle.gemm(x, qw, sc)
+    assert_w4_close(np.load(out), yr, ar, what="captured first M=8 call")
