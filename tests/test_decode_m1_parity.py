@@ -5,7 +5,10 @@ through the C ABI.
 The shapes cover the planner's choices: 8, 12 and 16 warps, one or two CTAs on
 an SM, one or several 16-row blocks per CTA with a shorter last CTA, sub-slices
 of equal and of unequal length, and group sizes 32 to 512; the decode sweep's
-longer shapes (served by the register-preload form) are checked here too.
+longer shapes (served by the shared-memory slot form) are checked here too,
+with the slot form's largest CTA (16 row blocks x 2 slices = its 32 slots),
+the same with a shorter last CTA, and the first shape past it (17 row blocks a
+CTA: the register-preload form).
 Bar: |y - y_ref| <= 1e-4 * sum|w x| + 1e-6 elementwise, and run to run bitwise
 identical results (fixed-order sums, no atomics).
 """
@@ -43,7 +46,8 @@ def _gemv(w4, x, qw, sc, group):
 SHAPES = [(2560, 1536), (1536, 2048), (12288, 1536), (1536, 6144), (24576, 1536), (1536, 12288),
           (2048, 2048), (256, 1536), (16, 128), (4096, 1536), (48, 384), (1536, 128),
           (2576, 1536), (1552, 6144), (3088, 3072), (784, 1024), (400, 6144), (32768, 2048),
-          (6160, 768), (1200, 8192), (784, 1152), (16, 1152)]
+          (6160, 768), (1200, 8192), (784, 1152), (16, 1152), (38912, 1536), (38896, 1536),
+          (38928, 1536)]
 
 
 @pytest.mark.parametrize("N,K", SHAPES)
