@@ -88,7 +88,9 @@ __device__ __forceinline__ uint32_t step_pair(const uint16_t *srow, int j, int l
 
 // The M <= 8 kernels' x staging (cpr == K / 8, every chunk real): all of a
 // thread's chunks in flight at once as asynchronous 16-byte copies, then the
-// pair permutation in place; the caller synchronises before use. At M = 8 and
+// pair permutation in place, each thread permuting the chunks it copied (its
+// own completed copies are visible to it, so no barrier sits between the two
+// passes); the caller synchronises before use. At M = 8 and
 // large K a thread stages up to 24 chunks, which the register path above
 // would fetch in six dependent round trips (measured on GB300: the M = 8
 // sweep 0.89 -> 0.82 ms, every shape faster in the sweep).
@@ -102,7 +104,6 @@ __device__ __forceinline__ void stage_x_rows_async(uint4 *xs, const uint16_t *x,
                      : "memory");
     asm volatile("cp.async.commit_group;" ::: "memory");
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncthreads();
     for (int i = threadIdx.x; i < total; i += blockDim.x)
         xs[i] = permute_x8(xs[i]);
 }
