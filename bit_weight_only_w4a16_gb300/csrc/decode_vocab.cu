@@ -404,11 +404,27 @@ w4_decode_slab_kernel(const VocabArgs a, int R, float norm, const __grid_constan
     pdl_launch_dependents();
     pdl_wait();
 
-    if (ROT)
+    if (ROT) {
         stage_x_hadamard<(ROT ? PL : 8)>(xs, a.x, a.K, nchunk, norm);
-    else
-        for (int i = threadIdx.x; i < nchunk; i += blockDim.x)
-            xs[i] = permute_x8(*reinterpret_cast<const uint4 *>(a.x + 8 * i));
+    } else {
+        // Up to kXL chunks of a thread in flight at once (6 a thread at
+        // K = 12288 with 8 warps): one memory round trip, not one per chunk.
+        constexpr int kXL = 6;
+        for (int i0 = threadIdx.x; i0 < nchunk; i0 += kXL * blockDim.x) {
+            uint4 v[kXL];
+#pragma unroll
+            for (int q = 0; q < kXL; ++q) {
+                const int i = i0 + q * blockDim.x;
+                v[q] = i < nchunk ? ldg_stream_v4(a.x + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int q = 0; q < kXL; ++q) {
+                const int i = i0 + q * blockDim.x;
+                if (i < nchunk)
+                    xs[i] = permute_x8(v[q]);
+            }
+        }
+    }
     if (threadIdx.x < 4)
         zs[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
